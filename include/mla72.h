@@ -1,0 +1,242 @@
+/*
+ * mla72.h - C ABI of the B300 (sm_103a) MLA absorbed-decode library.
+ *
+ * The operation is one decode step of Multi-head Latent Attention in its
+ * decode-time MQA form (kexue.fm "From MHA, MQA, GQA to MLA", section
+ * "Part 3", eq. mla-mqa): every head s of a sequence attends, with its
+ * absorbed query q_cat^(s) = [q_nope^(s) W_UK^(s), RoPE(q_rope^(s), pos)]
+ * (d_c + d_r = 576 values), over the cached rows k_i = [c_i, k_R,i]
+ * (the 512-d latent and the shared 64-d rotated RoPE key), with score scale
+ * 1/sqrt(d_nope + d_r) = 1/sqrt(192); the probabilities are applied to c_i,
+ * giving a 512-d latent output that W_UV maps to the 128-d value space
+ * (kexue.fm eq. mla-mqa, first line: o_t = [o^(s) W_v^(s)]).  Per-head keys
+ * and values are never formed.
+ *
+ * The step is four calls, all asynchronous on the caller's CUDA stream:
+ *   mla_absorb_q   -> q_cat            (W_UK folded into the query; RoPE of q_R)
+ *   mla_decode_fwd -> split partials   (online softmax over the latent cache)
+ *   mla_combine    -> o_lat, lse       (log-sum-exp merge of the splits)
+ *   mla_out_proj   -> out              (W_UV applied after attention)
+ * plus two preparation/test helpers (mla_cache_fill, mla_paged_gather).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or synchronises.  Arrays are dense, row-major, in
+ *     the shapes stated (last index fastest).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Host-side argument checks run before anything is launched; on failure
+ *     the call returns a negative mla_status and launches nothing.
+ *   - A CUDA launch error is returned as MLA_ERR_LAUNCH.
+ *   - Faults found on the device (a block-table entry outside the pool, a
+ *     bounded pipeline wait that ran out) are written to *dev_status where a
+ *     call takes one (0 = no fault; the word is only ever set, never cleared,
+ *     by the library); the offending access is skipped, never performed.
+ *   - No exception crosses the ABI.
+ */
+#ifndef MLA72_H
+#define MLA72_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+typedef enum {
+  MLA_F32 = 0,      /* IEEE binary32 */
+  MLA_BF16 = 1,     /* bfloat16 */
+  MLA_FP8E4M3 = 2   /* OCP FP8 E4M3 (latent cache only), one float32 scale per block */
+} mla_dtype;
+
+/* Return codes. */
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_ARG = -1,     /* null pointer, non-positive size, bad enum value */
+  MLA_ERR_ALIGN = -2,   /* a pointer or row stride is not 16-byte aligned */
+  MLA_ERR_DTYPE = -3,   /* unsupported dtype combination */
+  MLA_ERR_SHAPE = -4,   /* dimensions outside what the kernels support */
+  MLA_ERR_LAUNCH = -5,  /* CUDA reported an error at launch */
+  MLA_ERR_DEVICE = -6   /* no usable CUDA device / wrong architecture */
+} mla_status;
+
+/* Values a kernel may write to *dev_status. */
+#define MLA_DEV_OK 0
+#define MLA_DEV_BAD_BLOCK 1      /* block_table entry outside [0, num_blocks) */
+#define MLA_DEV_BAD_LENGTH 2     /* seq_len > max_blocks_per_seq * block_size */
+#define MLA_DEV_WAIT_TIMEOUT 3   /* a bounded pipeline wait gave up */
+
+/* Flags of mla_decode_fwd. */
+#define MLA_DECODE_AUTO 0u          /* tensor-core kernel where supported, else SIMT */
+#define MLA_DECODE_FORCE_SIMT 1u    /* always the CUDA-core (SIMT) kernel */
+
+/*
+ * Paged latent cache (iotdigitaltwinplm.com "Interaction with quantisation
+ * and paging": a page holds block_size * (d_c + d_r) elements per layer; the
+ * latent may be stored in FP8).  Token slot t of physical block p lives at
+ *   latent + (p * block_size + t) * latent_stride   (d_c elements)
+ *   rope   + (p * block_size + t) * rope_stride     (d_r elements, already rotated)
+ * (strides in elements of the respective dtype).  The packed bf16/f32 layout
+ * [num_blocks, block_size, d_c + d_r] is latent = pool, rope = pool + d_c,
+ * both strides d_c + d_r.  A contiguous per-sequence cache is the paged cache
+ * with an identity block table.  For MLA_FP8E4M3 latents, scale[p] is the
+ * float32 dequantisation scale of block p (value = e4m3(code) * scale[p]);
+ * scale is ignored otherwise and may be NULL.
+ */
+typedef struct {
+  void* latent;
+  void* rope;
+  float* scale;
+  int64_t latent_stride;
+  int64_t rope_stride;
+  int32_t latent_dtype;   /* mla_dtype */
+  int32_t rope_dtype;     /* mla_dtype: F32 or BF16 */
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t d_c;
+  int32_t d_r;
+} mla_kv_cache;
+
+/* Text for a status code (static storage). */
+const char* mla_status_string(int status);
+
+/* ABI version of this library (major * 100 + minor). */
+int mla_version(void);
+
+/*
+ * Bytes one cached token occupies per layer (iotdigitaltwinplm.com, "The
+ * Cache Arithmetic": MLA stores d_c + d_r elements per token per layer).  The
+ * FP8 per-block float32 scale is amortised over block_size tokens.
+ * Returns a negative value for an invalid combination.
+ */
+double mla_cache_bytes_per_token(int latent_dtype, int rope_dtype, int d_c, int d_r,
+                                 int block_size);
+
+/*
+ * mla_absorb_q: first step of the absorbed decode.
+ * kexue.fm section "Part 1" (q k^T = x (W_q W_k^T) c^T) and its note 2 (apply
+ * W_k^T to the already projected query, not a merged matrix); section "Part 3",
+ * eq. mla-mqa (q = [q_c W_kc^T, q_r R_t]); iotdigitaltwinplm.com, absorbed
+ * decode listing (q_lat = q . W_UK per head; RoPE of the rotary query part).
+ *
+ *   q_cat[b, s, c]       = sum_d q_nope[b, s, d] * w_uk[s, d, c]      c < d_c
+ *   q_cat[b, s, d_c + j] = RoPE(q_rope[b, s, :], q_pos[b])[j]           j < d_r
+ * RoPE rotates interleaved pairs (2i, 2i+1) by q_pos[b] * theta^(-2i/d_r)
+ * (angles formed in float64).  Accumulation is float32.
+ *
+ *   q_nope [B, h, d_nope], q_rope [B, h, d_r], w_uk [h, d_nope, d_c]: dtype
+ *   q_pos  [B] int32 (position of the decoded token)
+ *   q_cat  [B, h, d_c + d_r]: dtype (output)
+ * dtype is MLA_F32 or MLA_BF16 for all five float tensors.
+ * Supported: d_c % 64 == 0, d_c <= 1024, d_r even and <= 256, d_nope <= 512.
+ */
+int mla_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos,
+                 const void* w_uk, void* q_cat, int B, int h, int d_nope, int d_c, int d_r,
+                 int dtype, double rope_theta, void* stream);
+
+/*
+ * mla_decode_fwd: attention of each sequence's single query token over its
+ * cached latent rows (kexue.fm eq. mla-mqa, Attention(q_t, k_<=t, c_<=t);
+ * iotdigitaltwinplm.com absorbed decode listing: s = q_lat c^T + q_r k_R^T,
+ * softmax(s / sqrt(192)), ctx = p c).  Every cached row 0 .. seq_lens[b]-1 is
+ * visible to the query (it sits at the last position).
+ *
+ * Work of sequence b is cut into num_splits chunks of whole blocks: with
+ * nb = ceil(seq_lens[b] / block_size) and cb = ceil(nb / num_splits), split j
+ * covers logical blocks [j*cb, min((j+1)*cb, nb)).  For each (b, j, s):
+ *   o_part[b, j, s, :] = sum_i p_i c_i / sum_i p_i   over the split's rows
+ *   lse_part[b, j, s]  = log(sum_i exp(score_i))     (natural log, scaled scores)
+ * with score_i = softmax_scale * (q_cat[b, s, :] . [c_i, k_R,i]).  An empty
+ * split writes o_part = 0 and lse_part = -inf.
+ *
+ *   q_cat      [B, h, d_c + d_r]: q_dtype (MLA_F32 or MLA_BF16)
+ *   kv         cache descriptor (host pointer to the struct; its data pointers
+ *              are device pointers)
+ *   block_table[B, max_blocks_per_seq] int32: physical block of each logical block
+ *   seq_lens   [B] int32, each in [1, max_blocks_per_seq * block_size]
+ *   o_part     [B, num_splits, h, d_c] float32 (output)
+ *   lse_part   [B, num_splits, h] float32 (output)
+ *   dev_status int32 device word, may be NULL (see conventions)
+ *   flags      MLA_DECODE_AUTO or MLA_DECODE_FORCE_SIMT
+ * Supported dtypes: (q, latent, rope) = (F32, F32, F32) on the SIMT kernel;
+ * (BF16, BF16, BF16) and (BF16, FP8E4M3, BF16) on both kernels.  The tensor-core
+ * kernel runs for d_c = 512, d_r = 64, block_size = 64, h <= 128.
+ * softmax_scale <= 0 selects 1/sqrt(d_nope + d_r) with d_nope = 128.
+ */
+int mla_decode_fwd(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
+                   const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                   int B, int h, int num_splits, float softmax_scale, float* o_part,
+                   float* lse_part, int32_t* dev_status, unsigned flags, void* stream);
+
+/*
+ * mla_combine: merge the split partials of mla_decode_fwd (log-sum-exp
+ * weighting; the pages do not split the key range, this is the exact merge
+ * of softmax attention over disjoint key ranges):
+ *   M = max_j lse_part[b, j, s];  w_j = exp(lse_part[b, j, s] - M)
+ *   o_lat[b, s, :] = sum_j w_j o_part[b, j, s, :] / sum_j w_j
+ *   lse[b, s]      = M + log(sum_j w_j)
+ * Splits with lse = -inf get weight 0; if all are empty, o_lat = 0 and
+ * lse = -inf.
+ *   o_part [B, num_splits, h, d_c] f32, lse_part [B, num_splits, h] f32
+ *   o_lat  [B, h, d_c]: o_dtype (MLA_F32 or MLA_BF16) (output)
+ *   lse    [B, h] f32 (output, may be NULL)
+ * Supported: d_c % 4 == 0, d_c <= 2048.
+ */
+int mla_combine(const float* o_part, const float* lse_part, int B, int h, int d_c,
+                int num_splits, void* o_lat, int o_dtype, float* lse, void* stream);
+
+/*
+ * mla_out_proj: W_UV applied after attention (kexue.fm section "Part 1": W_v
+ * is absorbed into the projection that follows o_t; eq. mla-mqa first line
+ * o_t = [o^(1) W_v^(1), ..., o^(h) W_v^(h)]; iotdigitaltwinplm.com absorbed
+ * decode listing, out = ctx . W_UV per head):
+ *   out[b, s, v] = sum_c o_lat[b, s, c] * w_uv[s, v, c]
+ *   o_lat [B, h, d_c]: in_dtype;  w_uv [h, d_v, d_c]: in_dtype
+ *   out   [B, h, d_v]: out_dtype (output)
+ * in_dtype, out_dtype in {MLA_F32, MLA_BF16}.  Accumulation is float32.
+ * Supported: d_c % 64 == 0, d_c <= 1024, d_v <= 1024.
+ */
+int mla_out_proj(const void* o_lat, const void* w_uv, void* out, int B, int h, int d_c,
+                 int d_v, int in_dtype, int out_dtype, void* stream);
+
+/*
+ * mla_cache_fill: write whole sequences into the paged cache (the cache
+ * content of iotdigitaltwinplm.com's listing, appended rows c_t and
+ * RoPE(k_R, t); intvml.com: the RoPE key is cached in rotated form).
+ * Row t of sequence b (source row cu_seqlens[b] + t, 0 <= t < L_b with
+ * L_b = cu_seqlens[b+1] - cu_seqlens[b]) goes to physical block
+ * block_table[b, t / block_size], slot t % block_size:
+ *   latent row = c_kv row            (F32/BF16 cache: copied; FP8 cache: see below)
+ *   rope row   = RoPE(k_rope row, t) (angles t * theta^(-2i/d_r) in float64,
+ *                                     rotation in float32, stored in rope dtype)
+ * FP8 latent: per physical block, amax over the block's written rows and all
+ * d_c columns; scale = amax / 448 (float32 division; 1 if amax == 0);
+ * code = e4m3(c / scale) with the correctly rounded float32 quotient, rounding
+ * to nearest even and saturating to +-448; scale[p] is written.  Slots past
+ * L_b in a sequence's last block are not written.
+ *   c_kv [T, d_c]: src_dtype (MLA_F32, or MLA_BF16 for BF16/FP8 caches)
+ *   k_rope [T, d_r]: the cache's rope dtype
+ *   cu_seqlens [B + 1] int32 device array, T = cu_seqlens[B]
+ *   max_len: an upper bound of every L_b (sizes the launch)
+ * Block-table entries outside the pool are skipped and reported in *dev_status.
+ */
+int mla_cache_fill(const void* c_kv, const void* k_rope, int src_dtype,
+                   const int32_t* cu_seqlens, int B, int max_len, const int32_t* block_table,
+                   int max_blocks_per_seq, const mla_kv_cache* kv, double rope_theta,
+                   int32_t* dev_status, void* stream);
+
+/*
+ * mla_paged_gather: copy each sequence's logical rows out of the pool, bit for
+ * bit (latent in its stored dtype - e4m3 codes for FP8 - and the rotated rope).
+ *   latent_out [T, d_c], rope_out [T, d_r] (T = cu_seqlens[B]); either may be NULL.
+ */
+int mla_paged_gather(const mla_kv_cache* kv, const int32_t* block_table,
+                     int max_blocks_per_seq, const int32_t* cu_seqlens, int B, int max_len,
+                     void* latent_out, void* rope_out, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA72_H */

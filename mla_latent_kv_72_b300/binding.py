@@ -1,0 +1,207 @@
+"""ctypes binding of libmla72.so (see include/mla72.h for the contract).
+
+Functions carry the C names and take torch tensors; they pass data pointers,
+sizes and ``torch.cuda.current_stream()`` to the library and raise
+``MLAError`` on a non-zero status.  No arithmetic of the method happens here.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+MLA_F32 = 0
+MLA_BF16 = 1
+MLA_FP8E4M3 = 2
+
+MLA_DECODE_AUTO = 0
+MLA_DECODE_FORCE_SIMT = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+EXPORTED_SYMBOLS = (
+    "mla_status_string", "mla_version", "mla_cache_bytes_per_token", "mla_absorb_q",
+    "mla_decode_fwd", "mla_combine", "mla_out_proj", "mla_cache_fill", "mla_paged_gather",
+)
+
+
+class MLAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: status {status} ({mla_status_string(status)})")
+
+
+class KVCache(ctypes.Structure):
+    """ctypes mirror of ``mla_kv_cache`` (tensors kept alive on ``self.tensors``)."""
+
+    _fields_ = [
+        ("latent", ctypes.c_void_p),
+        ("rope", ctypes.c_void_p),
+        ("scale", ctypes.c_void_p),
+        ("latent_stride", ctypes.c_int64),
+        ("rope_stride", ctypes.c_int64),
+        ("latent_dtype", ctypes.c_int32),
+        ("rope_dtype", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("d_c", ctypes.c_int32),
+        ("d_r", ctypes.c_int32),
+    ]
+
+    @classmethod
+    def packed(cls, pool: torch.Tensor, d_c: int, d_r: int) -> "KVCache":
+        """Packed float pool [num_blocks, block_size, d_c + d_r] (latent then rope)."""
+        assert pool.dim() == 3 and pool.shape[2] == d_c + d_r and pool.is_contiguous()
+        dt = dtype_code(pool.dtype)
+        kv = cls(pool.data_ptr(), pool.data_ptr() + d_c * pool.element_size(), None,
+                 d_c + d_r, d_c + d_r, dt, dt, pool.shape[0], pool.shape[1], d_c, d_r)
+        kv.tensors = (pool,)
+        return kv
+
+    @classmethod
+    def split(cls, latent: torch.Tensor, rope: torch.Tensor,
+              scale: torch.Tensor | None = None) -> "KVCache":
+        """Separate pools: latent [nblk, bs, d_c] (bf16/f32, or uint8 e4m3 codes with
+        a float32 scale [nblk]) and rope [nblk, bs, d_r]."""
+        assert latent.is_contiguous() and rope.is_contiguous()
+        ldt = MLA_FP8E4M3 if latent.dtype in (torch.uint8, torch.float8_e4m3fn) else dtype_code(latent.dtype)
+        kv = cls(latent.data_ptr(), rope.data_ptr(), scale.data_ptr() if scale is not None else None,
+                 latent.shape[2], rope.shape[2], ldt, dtype_code(rope.dtype), latent.shape[0],
+                 latent.shape[1], latent.shape[2], rope.shape[2])
+        kv.tensors = (latent, rope, scale)
+        return kv
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libmla72.so")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmla72.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m mla_latent_kv_72_b300.build`")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, f32, f64, u32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                   ctypes.c_double, ctypes.c_uint)
+    kvp = ctypes.POINTER(KVCache)
+    sig = {
+        "mla_status_string": (ctypes.c_char_p, [i32]),
+        "mla_version": (i32, []),
+        "mla_cache_bytes_per_token": (f64, [i32, i32, i32, i32, i32]),
+        "mla_absorb_q": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f64, vp]),
+        "mla_decode_fwd": (i32, [vp, i32, kvp, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp, u32, vp]),
+        "mla_combine": (i32, [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp]),
+        "mla_out_proj": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
+        "mla_cache_fill": (i32, [vp, vp, i32, vp, i32, i32, vp, i32, kvp, f64, vp, vp]),
+        "mla_paged_gather": (i32, [kvp, vp, i32, vp, i32, i32, vp, vp, vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = L
+    return L
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return MLA_F32
+    if dt == torch.bfloat16:
+        return MLA_BF16
+    if dt in (torch.uint8, torch.float8_e4m3fn):
+        return MLA_FP8E4M3
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise MLAError(fn, status)
+
+
+def mla_status_string(status: int) -> str:
+    return lib().mla_status_string(status).decode()
+
+
+def mla_version() -> int:
+    return lib().mla_version()
+
+
+def mla_cache_bytes_per_token(latent_dtype: int, rope_dtype: int, d_c: int, d_r: int,
+                              block_size: int) -> float:
+    return lib().mla_cache_bytes_per_token(latent_dtype, rope_dtype, d_c, d_r, block_size)
+
+
+def mla_absorb_q(q_nope, q_rope, q_pos, w_uk, q_cat, rope_theta=10000.0, stream=None):
+    """q_cat[B, h, d_c + d_r] <- [q_nope W_UK, RoPE(q_rope, q_pos)] (see mla72.h)."""
+    B, h, d_nope = q_nope.shape
+    d_r = q_rope.shape[2]
+    d_c = w_uk.shape[2]
+    _check("mla_absorb_q", lib().mla_absorb_q(
+        _ptr(q_nope), _ptr(q_rope), _ptr(q_pos), _ptr(w_uk), _ptr(q_cat), B, h, d_nope, d_c, d_r,
+        dtype_code(q_nope.dtype), float(rope_theta), _stream(stream)))
+    return q_cat
+
+
+def mla_decode_fwd(q_cat, kv: KVCache, block_table, seq_lens, o_part, lse_part, *,
+                   softmax_scale=0.0, dev_status=None, flags=MLA_DECODE_AUTO, stream=None):
+    """Split-KV partials o_part [B, S, h, d_c], lse_part [B, S, h] (see mla72.h)."""
+    B, h, _ = q_cat.shape
+    num_splits = o_part.shape[1]
+    _check("mla_decode_fwd", lib().mla_decode_fwd(
+        _ptr(q_cat), dtype_code(q_cat.dtype), ctypes.byref(kv), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, h, num_splits, float(softmax_scale),
+        _ptr(o_part), _ptr(lse_part), _ptr(dev_status), int(flags), _stream(stream)))
+
+
+def mla_combine(o_part, lse_part, o_lat, lse=None, stream=None):
+    """o_lat [B, h, d_c], lse [B, h] from the split partials (see mla72.h)."""
+    B, S, h, d_c = o_part.shape
+    _check("mla_combine", lib().mla_combine(
+        _ptr(o_part), _ptr(lse_part), B, h, d_c, S, _ptr(o_lat), dtype_code(o_lat.dtype),
+        _ptr(lse), _stream(stream)))
+    return o_lat
+
+
+def mla_out_proj(o_lat, w_uv, out, stream=None):
+    """out[b, s, v] = sum_c o_lat[b, s, c] w_uv[s, v, c] (see mla72.h)."""
+    B, h, d_c = o_lat.shape
+    d_v = w_uv.shape[1]
+    _check("mla_out_proj", lib().mla_out_proj(
+        _ptr(o_lat), _ptr(w_uv), _ptr(out), B, h, d_c, d_v, dtype_code(o_lat.dtype),
+        dtype_code(out.dtype), _stream(stream)))
+    return out
+
+
+def mla_cache_fill(c_kv, k_rope, cu_seqlens, max_len, block_table, kv: KVCache,
+                   rope_theta=10000.0, dev_status=None, stream=None):
+    """Write rows of B sequences into the paged cache (see mla72.h)."""
+    B = cu_seqlens.shape[0] - 1
+    _check("mla_cache_fill", lib().mla_cache_fill(
+        _ptr(c_kv), _ptr(k_rope), dtype_code(c_kv.dtype), _ptr(cu_seqlens), B, int(max_len),
+        _ptr(block_table), block_table.shape[1], ctypes.byref(kv), float(rope_theta),
+        _ptr(dev_status), _stream(stream)))
+
+
+def mla_paged_gather(kv: KVCache, block_table, cu_seqlens, max_len, latent_out=None,
+                     rope_out=None, dev_status=None, stream=None):
+    """Bit-exact logical rows out of the pool (see mla72.h)."""
+    B = cu_seqlens.shape[0] - 1
+    _check("mla_paged_gather", lib().mla_paged_gather(
+        ctypes.byref(kv), _ptr(block_table), block_table.shape[1], _ptr(cu_seqlens), B,
+        int(max_len), _ptr(latent_out), _ptr(rope_out), _ptr(dev_status), _stream(stream)))

@@ -1,0 +1,100 @@
+// mla_combine: log-sum-exp merge of the split-KV partials.
+//
+// Exact merge of softmax attention computed over disjoint key ranges: each
+// range's normalised output is weighted by exp(lse_j - max_j lse_j).
+#include <math.h>
+
+#include "common.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kMaxSplits = 1024;
+
+// grid: (h, B); block: 128 threads, each owning 4 consecutive latent columns per pass.
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int B, int h,
+               int d_c, int num_splits, void* __restrict__ o_lat, int o_dtype,
+               float* __restrict__ lse_out) {
+  __shared__ float sw[kMaxSplits];
+  __shared__ float s_m, s_inv, s_lse;
+  const int s = blockIdx.x, b = blockIdx.y;
+  const int64_t lbase = (int64_t)b * num_splits * h + s;   // lse_part[b, j, s] = lbase + j*h
+
+  // maximum over splits
+  float m = -INFINITY;
+  for (int j = threadIdx.x; j < num_splits; j += kThreads) m = fmaxf(m, lse_part[lbase + (int64_t)j * h]);
+  __shared__ float red[kThreads / 32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mm = red[0];
+    for (int w = 1; w < kThreads / 32; ++w) mm = fmaxf(mm, red[w]);
+    s_m = mm;
+  }
+  __syncthreads();
+  m = s_m;
+  // weights
+  float wsum = 0.f;
+  for (int j = threadIdx.x; j < num_splits; j += kThreads) {
+    float l = lse_part[lbase + (int64_t)j * h];
+    float w = (m == -INFINITY || l == -INFINITY) ? 0.f : expf(l - m);
+    sw[j] = w;
+    wsum += w;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+  __syncthreads();
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = wsum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) t += red[w];
+    s_inv = t > 0.f ? 1.f / t : 0.f;
+    s_lse = t > 0.f ? m + logf(t) : -INFINITY;
+  }
+  __syncthreads();
+  const float inv = s_inv;
+
+  const int64_t obase = ((int64_t)b * h + s) * d_c;
+  for (int c = threadIdx.x * 4; c < d_c; c += kThreads * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < num_splits; ++j) {
+      float w = sw[j];
+      if (w == 0.f) continue;
+      const float4 v = *reinterpret_cast<const float4*>(
+          o_part + (((int64_t)b * num_splits + j) * h + s) * d_c + c);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    if (o_dtype == MLA_F32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(o_lat) + obase + c) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      uint16_t* o = static_cast<uint16_t*>(o_lat) + obase + c;
+      uint2 pk;
+      pk.x = (uint32_t)f32_to_bf16_rn(acc.x * inv) | ((uint32_t)f32_to_bf16_rn(acc.y * inv) << 16);
+      pk.y = (uint32_t)f32_to_bf16_rn(acc.z * inv) | ((uint32_t)f32_to_bf16_rn(acc.w * inv) << 16);
+      *reinterpret_cast<uint2*>(o) = pk;
+    }
+  }
+  if (lse_out && threadIdx.x == 0) lse_out[(int64_t)b * h + s] = s_lse;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int h, int d_c,
+                           int num_splits, void* o_lat, int o_dtype, float* lse, cudaStream_t s) {
+  if (num_splits > kMaxSplits) return cudaErrorInvalidValue;
+  dim3 grid(h, B);
+  combine_kernel<<<grid, kThreads, 0, s>>>(o_part, lse_part, B, h, d_c, num_splits, o_lat,
+                                           o_dtype, lse);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

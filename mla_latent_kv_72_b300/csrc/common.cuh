@@ -1,0 +1,110 @@
+// Shared device helpers and internal launcher declarations of the MLA library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/mla72.h"
+
+namespace mla {
+
+// ---------------------------------------------------------------------------
+// element access
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// e4m3 code -> float (exact)
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+  __nv_fp8_e4m3 v;
+  v.__x = c;
+  return static_cast<float>(v);
+}
+
+// float -> e4m3 code, round to nearest even, saturate to +-448
+__device__ __forceinline__ uint8_t f32_to_e4m3_rn_sat(float f) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(f, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Load element i of an array of the given dtype as float.
+__device__ __forceinline__ float load_as_f32(const void* p, int dtype, int64_t i) {
+  if (dtype == MLA_F32) return static_cast<const float*>(p)[i];
+  if (dtype == MLA_BF16) return bf16_to_f32(static_cast<const uint16_t*>(p)[i]);
+  return e4m3_to_f32(static_cast<const uint8_t*>(p)[i]);
+}
+
+__device__ __forceinline__ void store_from_f32(void* p, int dtype, int64_t i, float v) {
+  if (dtype == MLA_F32) {
+    static_cast<float*>(p)[i] = v;
+  } else {
+    static_cast<uint16_t*>(p)[i] = f32_to_bf16_rn(v);
+  }
+}
+
+__device__ __forceinline__ void set_status(int32_t* st, int code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+__host__ __device__ __forceinline__ int dtype_bytes(int dt) {
+  return dt == MLA_F32 ? 4 : (dt == MLA_BF16 ? 2 : 1);
+}
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Logical block range [lo, hi) of split j for a sequence of nb blocks.
+__host__ __device__ __forceinline__ void split_range(int nb, int num_splits, int j, int* lo,
+                                                     int* hi) {
+  int cb = ceil_div(nb, num_splits);
+  int a = j * cb;
+  int e = a + cb;
+  *lo = a < nb ? a : nb;
+  *hi = e < nb ? e : nb;
+}
+
+// ---------------------------------------------------------------------------
+// internal launchers (one per kernel family); each returns cudaError_t
+// ---------------------------------------------------------------------------
+
+cudaError_t launch_absorb_q_simt(const void* q_nope, const void* q_rope, const int32_t* q_pos,
+                                 const void* w_uk, void* q_cat, int B, int h, int d_nope,
+                                 int d_c, int d_r, int dtype, double theta, cudaStream_t s);
+
+cudaError_t launch_decode_simt(const void* q_cat, int q_dtype, const mla_kv_cache& kv,
+                               const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                               int B, int h, int num_splits, float scale, float* o_part,
+                               float* lse_part, int32_t* status, cudaStream_t s);
+
+bool decode_tc_supported(int q_dtype, const mla_kv_cache& kv, int h);
+
+cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
+                             const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                             int B, int h, int num_splits, float scale, float* o_part,
+                             float* lse_part, int32_t* status, cudaStream_t s);
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int h, int d_c,
+                           int num_splits, void* o_lat, int o_dtype, float* lse, cudaStream_t s);
+
+cudaError_t launch_out_proj_simt(const void* o_lat, const void* w_uv, void* out, int B, int h,
+                                 int d_c, int d_v, int in_dtype, int out_dtype, cudaStream_t s);
+
+cudaError_t launch_cache_fill(const void* c_kv, const void* k_rope, int src_dtype,
+                              const int32_t* cu_seqlens, int B, int max_len,
+                              const int32_t* block_table, int max_blocks,
+                              const mla_kv_cache& kv, double theta, int32_t* status,
+                              cudaStream_t s);
+
+cudaError_t launch_paged_gather(const mla_kv_cache& kv, const int32_t* block_table,
+                                int max_blocks, const int32_t* cu_seqlens, int B, int max_len,
+                                void* latent_out, void* rope_out, int32_t* status,
+                                cudaStream_t s);
+
+}  // namespace mla

@@ -1,0 +1,164 @@
+"""Device-resident state of one decode workload, built from the seeded inputs.
+
+Uploads the seeded queries and weights, allocates the paged cache pool, and
+writes every sequence into it with ``mla_cache_fill`` (NaN-poisoned tail
+slots).  ``step()`` runs one decode step through the four C-ABI calls.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import mla_inputs as mi
+
+from . import binding as C
+
+
+def storage_to_torch(a: np.ndarray, dtype: str, device) -> torch.Tensor:
+    """numpy storage array (bf16 bits as uint16, or float32) -> torch tensor on device."""
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    elif dtype == "f32":
+        t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    else:
+        raise ValueError(dtype)
+    return t.to(device)
+
+
+def choose_num_splits(B: int, max_len: int, block_size: int, num_sms: int, heads_ctas: int = 1) -> int:
+    """Split count so that B * splits * heads_ctas fills the SMs about twice (capped
+    so that a split keeps at least 4 blocks)."""
+    nb = max(1, (max_len + block_size - 1) // block_size)
+    want = max(1, (2 * num_sms + B * heads_ctas - 1) // (B * heads_ctas))
+    return int(max(1, min(want, nb // 4 if nb >= 4 else 1, 1024)))
+
+
+class DeviceWorkload:
+    """Everything one decode step reads and writes, resident on one GPU."""
+
+    def __init__(self, w: mi.Workload, device="cuda", num_splits: int | None = None,
+                 rows_per_upload: int = 1 << 20, out_dtype=torch.float32):
+        self.w = w
+        self.device = torch.device(device)
+        dev = self.device
+        lens = mi.lengths(w)
+        table, nblk = mi.block_table(w, lens)
+        self.lens_np = lens
+        self.table_np = table
+        self.num_blocks = nblk
+        self.max_len = int(lens.max())
+        tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+
+        qn, qr = mi.queries(w)
+        wuk, wuv = mi.weights(w)
+        self.q_nope = storage_to_torch(qn, w.dtype, dev)
+        self.q_rope = storage_to_torch(qr, w.dtype, dev)
+        self.w_uk = storage_to_torch(wuk, w.dtype, dev)
+        self.w_uv = storage_to_torch(wuv, w.dtype, dev)
+        self.q_pos = torch.from_numpy(mi.query_positions(w, lens)).to(dev)
+        self.seq_lens = torch.from_numpy(lens.astype(np.int32)).to(dev)
+        self.block_table = torch.from_numpy(table).to(dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        # cache pool, tails poisoned with NaN
+        bs, d_c, d_r = w.block_size, w.d_c, w.d_r
+        if w.latent_dtype == "fp8e4m3":
+            self.latent = torch.full((nblk, bs, d_c), 0x7F, dtype=torch.uint8, device=dev)
+            self.rope = torch.full((nblk, bs, d_r), float("nan"), dtype=torch.bfloat16, device=dev)
+            self.scale = torch.full((nblk,), float("nan"), dtype=torch.float32, device=dev)
+            self.kv = C.KVCache.split(self.latent, self.rope, self.scale)
+            self.pool = None
+        else:
+            self.pool = torch.full((nblk, bs, d_c + d_r), float("nan"), dtype=tdt, device=dev)
+            self.kv = C.KVCache.packed(self.pool, d_c, d_r)
+        self._fill(rows_per_upload)
+
+        if num_splits is None:
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            num_splits = choose_num_splits(w.B, self.max_len, bs, sms)
+        self.num_splits = num_splits
+        B, h = w.B, w.h
+        self.q_cat = torch.empty((B, h, d_c + d_r), dtype=tdt, device=dev)
+        self.o_part = torch.empty((B, num_splits, h, d_c), dtype=torch.float32, device=dev)
+        self.lse_part = torch.empty((B, num_splits, h), dtype=torch.float32, device=dev)
+        self.o_lat = torch.empty((B, h, d_c), dtype=tdt, device=dev)
+        self.lse = torch.empty((B, h), dtype=torch.float32, device=dev)
+        self.out = torch.empty((B, h, w.d_v), dtype=out_dtype, device=dev)
+
+    # -- cache -------------------------------------------------------------
+    def _fill(self, rows_per_upload: int) -> None:
+        w = self.w
+        src_dt = mi.latent_source_dtype(w)
+        b = 0
+        while b < w.B:
+            e, rows = b, 0
+            while e < w.B and (e == b or rows + self.lens_np[e] <= rows_per_upload):
+                rows += int(self.lens_np[e])
+                e += 1
+            cs, krs = [], []
+            for bb in range(b, e):
+                c, kr = mi.sequence(w, bb, int(self.lens_np[bb]))
+                cs.append(c)
+                krs.append(kr)
+            c_t = storage_to_torch(np.concatenate(cs), src_dt, self.device)
+            kr_t = storage_to_torch(np.concatenate(krs), w.dtype, self.device)
+            cu = np.zeros(e - b + 1, dtype=np.int32)
+            cu[1:] = np.cumsum(self.lens_np[b:e])
+            cu_t = torch.from_numpy(cu).to(self.device)
+            tab = self.block_table[b:e].contiguous()
+            C.mla_cache_fill(c_t, kr_t, cu_t, int(self.lens_np[b:e].max()), tab, self.kv,
+                             rope_theta=w.theta, dev_status=self.status)
+            b = e
+        torch.cuda.synchronize(self.device)
+
+    # -- the decode step ---------------------------------------------------
+    def absorb(self, stream=None):
+        C.mla_absorb_q(self.q_nope, self.q_rope, self.q_pos, self.w_uk, self.q_cat,
+                       rope_theta=self.w.theta, stream=stream)
+
+    def attend(self, flags=C.MLA_DECODE_AUTO, stream=None):
+        C.mla_decode_fwd(self.q_cat, self.kv, self.block_table, self.seq_lens, self.o_part,
+                         self.lse_part, dev_status=self.status, flags=flags, stream=stream)
+
+    def combine(self, stream=None):
+        C.mla_combine(self.o_part, self.lse_part, self.o_lat, self.lse, stream=stream)
+
+    def project(self, stream=None):
+        C.mla_out_proj(self.o_lat, self.w_uv, self.out, stream=stream)
+
+    def step(self, flags=C.MLA_DECODE_AUTO, stream=None):
+        self.absorb(stream)
+        self.attend(flags, stream)
+        self.combine(stream)
+        self.project(stream)
+        return self.out
+
+    # -- bookkeeping -------------------------------------------------------
+    def cache_bytes(self) -> float:
+        """Algorithmic bytes of the cache one step reads: sum_b L_b * bytes/token."""
+        w = self.w
+        per_tok = C.mla_cache_bytes_per_token(
+            {"f32": 0, "bf16": 1, "fp8e4m3": 2}[w.latent_dtype],
+            0 if w.dtype == "f32" else 1, w.d_c, w.d_r, w.block_size)
+        return float(self.lens_np.sum()) * per_tok
+
+    def step_bytes(self) -> float:
+        """Algorithmic bytes of one full step (cache, queries, weights, outputs)."""
+        w = self.w
+        el = 4 if w.dtype == "f32" else 2
+        B, h = w.B, w.h
+        q_in = B * h * (w.d_nope + w.d_r) * el
+        wts = 2 * h * w.d_v * w.d_c * el
+        table = self.table_np.size * 4 + B * 4
+        out = B * h * w.d_v * self.out.element_size()
+        return self.cache_bytes() + q_in + wts + table + out
+
+    def step_flops(self) -> float:
+        """2 * h * (d_c + d_r + d_c) per cached token, plus the two per-head GEMMs."""
+        w = self.w
+        attn = float(self.lens_np.sum()) * w.h * 2 * (w.d_c + w.d_r + w.d_c)
+        gemms = 2.0 * w.B * w.h * w.d_c * (w.d_nope + w.d_v)
+        return attn + gemms
+
+    def check_status(self) -> int:
+        return int(self.status.item())

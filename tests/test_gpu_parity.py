@@ -1,0 +1,257 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Tolerance (stated by the task's target): max|err| / max|ref| <= 1e-4 for the
+float32 workload and <= 2e-2 for bf16 / FP8 workloads, on the output after
+W_UV and on the latent output; paged gathers are bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs as mi
+import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_latent_kv_72_b300 import build
+    build.build()
+
+
+def rel_err(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), "non-finite values in the GPU result"
+    return float(np.abs(got - ref).max() / np.abs(ref).max())
+
+
+def oracle_for(w, batch, heads=None):
+    inp = O.workload_inputs_f64(w)
+    seqs = [O.sequence_view(w, b, int(inp["lens"][b])) for b in batch]
+    idx = list(batch)
+    return O.decode_reference(inp["q_nope"][idx], inp["q_rope"][idx], inp["q_pos"][idx],
+                              inp["w_uk"], inp["w_uv"], seqs, heads=heads)
+
+
+def make(w, **kw):
+    from mla_latent_kv_72_b300.workload import DeviceWorkload
+    return DeviceWorkload(w, **kw)
+
+
+def compare(w, dw, batch, heads, tol):
+    ref = oracle_for(w, batch, heads)
+    hs = list(range(w.h)) if heads is None else list(heads)
+    out = dw.out.float().cpu().numpy()[np.ix_(list(batch), hs)]
+    o_lat = dw.o_lat.float().cpu().numpy()[np.ix_(list(batch), hs)]
+    lse = dw.lse.float().cpu().numpy()[np.ix_(list(batch), hs)]
+    e_out = rel_err(out, ref["out"])
+    e_lat = rel_err(o_lat, ref["o_lat"])
+    e_lse = rel_err(lse, ref["lse"])
+    assert e_out <= tol, ("out", e_out)
+    assert e_lat <= tol, ("o_lat", e_lat)
+    assert e_lse <= tol, ("lse", e_lse)
+    return e_out, e_lat, e_lse
+
+
+# ----------------------------------------------------------------------------
+# whole workloads, small enough for the oracle to check every output
+# ----------------------------------------------------------------------------
+
+SMALL_CASES = {
+    "tiny_fp32_full": mi.workload(1),
+    "small_bf16_ragged": mi.scaled(mi.workload(2), B=3, L=1000),
+    "v3_bf16_two_seqs": mi.scaled(mi.workload(3), B=2, L=700),
+    "paged_bf16_ragged": mi.scaled(mi.workload(4), B=6, L_range=(1, 700)),
+    "fp8_bf16_long": mi.scaled(mi.workload(5), B=2, L=2500),
+}
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["auto", "simt"])
+@pytest.mark.parametrize("name", list(SMALL_CASES))
+def test_small_workloads_match_oracle(name, flags):
+    w = SMALL_CASES[name]
+    dw = make(w)
+    dw.step(flags=flags)
+    torch.cuda.synchronize()
+    assert dw.check_status() == 0
+    tol = TOL["f32" if w.dtype == "f32" else "bf16"]
+    compare(w, dw, range(w.B), None, tol)
+
+
+@pytest.mark.parametrize("L", [1, 2, 63, 64, 65, 129])
+def test_edge_lengths(L):
+    w = mi.scaled(mi.workload(3), B=2, h=16, L=L)
+    for ns in (1, 3):
+        dw = make(w, num_splits=ns)
+        dw.step()
+        torch.cuda.synchronize()
+        compare(w, dw, range(w.B), None, TOL["bf16"])
+
+
+def test_fp32_tolerance_is_tight():
+    # the float32 workload must sit well inside 1e-4
+    w = mi.workload(1)
+    dw = make(w)
+    dw.step()
+    torch.cuda.synchronize()
+    e = compare(w, dw, range(w.B), None, TOL["f32"])
+    assert max(e) < 1e-5
+
+
+# ----------------------------------------------------------------------------
+# split-KV and paging invariants
+# ----------------------------------------------------------------------------
+
+def test_split_count_invariance():
+    w = mi.scaled(mi.workload(3), B=2, h=128, L=3000)
+    ref = None
+    for ns in (1, 2, 7, 64):
+        dw = make(w, num_splits=ns)
+        dw.step()
+        torch.cuda.synchronize()
+        o = dw.o_lat.float().cpu().numpy()
+        if ref is None:
+            ref = o
+        else:
+            assert np.abs(o - ref).max() / np.abs(ref).max() < 1e-2
+    compare(w, dw, range(w.B), [0, 77, 127], TOL["bf16"])
+
+
+def test_paged_permutation_is_bit_exact():
+    base = mi.scaled(mi.workload(4), B=4, L_range=(100, 900))
+    contig = mi.scaled(base, layout="contiguous")
+    a = make(base, num_splits=3)
+    b = make(contig, num_splits=3)
+    assert not np.array_equal(a.table_np, b.table_np)
+    for dw in (a, b):
+        dw.step()
+    torch.cuda.synchronize()
+    assert torch.equal(a.o_part.view(torch.int32), b.o_part.view(torch.int32))
+    assert torch.equal(a.out.view(torch.int32), b.out.view(torch.int32))
+
+
+def test_empty_splits_are_harmless():
+    w = mi.scaled(mi.workload(3), B=2, h=16, L=100)      # 2 blocks, 16 splits
+    dw = make(w, num_splits=16)
+    dw.step()
+    torch.cuda.synchronize()
+    lse_part = dw.lse_part.cpu().numpy()
+    assert np.isneginf(lse_part).any()
+    compare(w, dw, range(w.B), None, TOL["bf16"])
+
+
+def test_bad_block_is_reported_not_dereferenced():
+    w = mi.scaled(mi.workload(3), B=2, h=16, L=200)
+    dw = make(w, num_splits=1)
+    dw.block_table[1, 1] = dw.num_blocks + 1000
+    dw.step()
+    torch.cuda.synchronize()
+    from mla_latent_kv_72_b300 import binding
+    assert dw.check_status() == 1          # MLA_DEV_BAD_BLOCK
+    dw.status.zero_()
+    dw.step(flags=binding.MLA_DECODE_FORCE_SIMT)
+    torch.cuda.synchronize()
+    assert dw.check_status() == 1
+
+
+# ----------------------------------------------------------------------------
+# the cache writer and the gather
+# ----------------------------------------------------------------------------
+
+def _gather(dw):
+    from mla_latent_kv_72_b300 import binding as C
+    w = dw.w
+    T = int(dw.lens_np.sum())
+    cu = np.zeros(w.B + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(dw.lens_np)
+    ldt = torch.uint8 if w.latent_dtype == "fp8e4m3" else (torch.float32 if w.dtype == "f32" else torch.bfloat16)
+    lat = torch.empty((T, w.d_c), dtype=ldt, device="cuda")
+    rope = torch.empty((T, w.d_r), dtype=torch.float32 if w.dtype == "f32" else torch.bfloat16,
+                       device="cuda")
+    C.mla_paged_gather(dw.kv, dw.block_table, torch.from_numpy(cu).cuda(), dw.max_len, lat, rope,
+                       dev_status=dw.status)
+    torch.cuda.synchronize()
+    return lat.cpu(), rope.float().cpu().numpy(), cu
+
+
+@pytest.mark.parametrize("idx", [1, 4, 5])
+def test_cache_fill_and_gather(idx):
+    w = mi.scaled(mi.workload(idx), B=3, L=None, L_range=(1, 300)) if idx == 4 else \
+        mi.scaled(mi.workload(idx), B=2, L=200)
+    dw = make(w)
+    lat, rope, cu = _gather(dw)
+    assert dw.check_status() == 0
+    src_dt = mi.latent_source_dtype(w)
+    for b in range(w.B):
+        L = int(dw.lens_np[b])
+        c_src, kr_src = mi.sequence(w, b, L)
+        got = lat[cu[b]:cu[b + 1]]
+        if w.latent_dtype == "fp8e4m3":
+            c32 = mi.storage_to_f64(c_src, src_dt).astype(np.float32)
+            codes, scales, _ = O.quantized_latent_f64(c32, w.block_size)
+            np.testing.assert_array_equal(got.numpy(), codes)          # bit-exact codes
+            sc = dw.scale.cpu().numpy()[dw.table_np[b, : len(scales)]]
+            np.testing.assert_array_equal(sc, scales)
+        elif w.dtype == "bf16":
+            np.testing.assert_array_equal(got.view(torch.int16).numpy().view(np.uint16), c_src)
+        else:
+            np.testing.assert_array_equal(got.numpy(), c_src)
+        # rotated key against the float64 rotation of the same pre-image
+        kr_ref = O.rope(mi.storage_to_f64(kr_src, w.dtype), np.arange(L))
+        ulp = 2.0 ** -7 if w.dtype == "bf16" else 2.0 ** -20
+        assert np.all(np.abs(rope[cu[b]:cu[b + 1]] - kr_ref) <= ulp * np.abs(kr_ref) + 1e-6)
+
+
+def test_absorb_q_matches_oracle():
+    for idx in (1, 3):
+        w = mi.scaled(mi.workload(idx), B=5) if idx == 3 else mi.workload(idx)
+        dw = make(w)
+        dw.absorb()
+        torch.cuda.synchronize()
+        inp = O.workload_inputs_f64(w)
+        ref = O.absorb_query(inp["q_nope"], inp["q_rope"], inp["q_pos"], inp["w_uk"])
+        got = dw.q_cat.float().cpu().numpy()
+        tol = 1e-5 if w.dtype == "f32" else 1e-2
+        assert rel_err(got[..., :512], ref[..., :512]) < tol
+        assert rel_err(got[..., 512:], ref[..., 512:]) < tol
+
+
+def test_out_proj_matches_oracle():
+    w = mi.scaled(mi.workload(3), B=5)
+    dw = make(w)
+    g = torch.Generator(device="cpu").manual_seed(0)
+    o_lat = torch.randn((w.B, w.h, w.d_c), generator=g).to(torch.bfloat16)
+    dw.o_lat.copy_(o_lat)
+    dw.project()
+    torch.cuda.synchronize()
+    inp = O.workload_inputs_f64(w)
+    ref = O.output_projection(o_lat.double().numpy(), inp["w_uv"])
+    assert rel_err(dw.out.float().cpu().numpy(), ref) < 1e-3
+
+
+# ----------------------------------------------------------------------------
+# full-size workloads: sampled outputs, computed one by one by the oracle
+# ----------------------------------------------------------------------------
+
+SAMPLES = {2: [(0, 0), (31, 7), (63, 15)],
+           3: [(0, 0), (17, 64), (63, 127)],
+           4: [(0, 3), (64, 100), (127, 127)],
+           5: [(0, 0), (3, 127)]}
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4, 5])
+def test_full_size_sampled(idx):
+    w = mi.workload(idx)
+    dw = make(w)
+    dw.step()
+    torch.cuda.synchronize()
+    assert dw.check_status() == 0
+    assert torch.isfinite(dw.out).all()
+    for b, s in SAMPLES[idx]:
+        compare(w, dw, [b], [s], TOL["bf16"])
