@@ -344,8 +344,8 @@ def run_ours(args) -> None:
 
     step_bytes = dw.step_bytes()
     step_flops = dw.step_flops()
-    value = aggregate(step_bytes, world, max_total) / 1e9
-    tflops = aggregate(step_flops, world, max_total) / 1e12
+    value = aggregate(step_bytes * args.steps, world, max_total) / 1e9
+    tflops = aggregate(step_flops * args.steps, world, max_total) / 1e12
 
     # end to end through the C ABI: pinned host inputs in, output back, every step
     h_qn = dw.q_nope.cpu().pin_memory()
