@@ -278,10 +278,10 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
-def bench_config(w, num_splits) -> dict:
+def bench_config(w, num_parts) -> dict:
     return {"workload": w.name, "B": w.B, "h": w.h, "L": w.L, "d_c": w.d_c, "d_r": w.d_r,
             "d_nope": w.d_nope, "d_v": w.d_v, "cache_dtype": w.latent_dtype,
-            "block_size": w.block_size, "num_splits": num_splits,
+            "block_size": w.block_size, "num_parts": num_parts,
             "l2": "inputs larger than L2 (604 MB latent cache per step)",
             "parallelism": "independent replica per GPU (batch-parallel, no collective)"}
 
@@ -308,7 +308,7 @@ def run_ours(args) -> None:
     barrier()
     C.lib()
     w = mi.workload(WORKLOAD)
-    dw = DeviceWorkload(w, device=f"cuda:{local}", num_splits=args.splits)
+    dw = DeviceWorkload(w, device=f"cuda:{local}", num_parts=args.parts)
     stream = torch.cuda.current_stream()
 
     # warm-up
@@ -398,7 +398,7 @@ def run_ours(args) -> None:
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": bench_config(w, dw.num_splits),
+        "data": "synthetic", "config": bench_config(w, dw.num_parts),
         "tflops": tflops, "steps_per_s": args.steps / max_total,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
@@ -421,7 +421,8 @@ def main(argv=None) -> None:
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--splits", type=int, default=None, help="split-KV chunks per sequence")
+    p.add_argument("--parts", type=int, default=None,
+                   help="balanced parts of the block stream (default: half the SM count)")
     p.add_argument("--cpu-budget", type=float, default=15.0,
                    help="seconds of oracle work for the CPU baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -14,7 +14,8 @@
  *
  * The step is four calls, all asynchronous on the caller's CUDA stream:
  *   mla_absorb_q   -> q_cat            (W_UK folded into the query; RoPE of q_R)
- *   mla_decode_fwd -> split partials   (online softmax over the latent cache)
+ *   mla_decode_fwd -> partials         (online softmax over the latent cache,
+ *                                       balanced parts of all sequences' blocks)
  *   mla_combine    -> o_lat, lse       (log-sum-exp merge of the splits)
  *   mla_out_proj   -> out              (W_UV applied after attention)
  * plus two preparation/test helpers (mla_cache_fill, mla_paged_gather).
@@ -135,6 +136,27 @@ int mla_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos,
                  const void* w_uk, void* q_cat, int B, int h, int d_nope, int d_c, int d_r,
                  int dtype, double rope_theta, void* stream);
 
+/* Largest num_parts accepted by mla_decode_fwd / mla_combine. */
+#define MLA_MAX_PARTS 1024
+
+/*
+ * Work partition shared by mla_decode_fwd and mla_combine (not on the pages:
+ * it only decides which key ranges are attended separately; the merge in
+ * mla_combine is exact).  The logical blocks of all sequences, in order
+ * (sequence 0's ceil(L_0 / block_size) blocks, then sequence 1's, ...), form
+ * one stream of T blocks, L_b = seq_lens[b] clamped to
+ * [0, max_blocks_per_seq * block_size].  With P = min(num_parts, T), part p
+ * covers stream blocks [floor(p T / P), floor((p + 1) T / P)): parts are
+ * contiguous, non-empty and balanced to within one block, whatever the
+ * length mix.  A part writes one partial result for each sequence b it
+ * touches, into partial slot p + b (unique, since parts and sequences are
+ * both ordered along the stream).  Slots no part touches are not written.
+ *
+ * mla_decode_num_partials: number of partial slots, B + num_parts - 1, or a
+ * negative mla_status for invalid arguments.
+ */
+int mla_decode_num_partials(int B, int num_parts);
+
 /*
  * mla_decode_fwd: attention of each sequence's single query token over its
  * cached latent rows (kexue.fm eq. mla-mqa, Attention(q_t, k_<=t, c_<=t);
@@ -142,49 +164,53 @@ int mla_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos,
  * softmax(s / sqrt(192)), ctx = p c).  Every cached row 0 .. seq_lens[b]-1 is
  * visible to the query (it sits at the last position).
  *
- * Work of sequence b is cut into num_splits chunks of whole blocks: with
- * nb = ceil(seq_lens[b] / block_size) and cb = ceil(nb / num_splits), split j
- * covers logical blocks [j*cb, min((j+1)*cb, nb)).  For each (b, j, s):
- *   o_part[b, j, s, :] = sum_i p_i c_i / sum_i p_i   over the split's rows
- *   lse_part[b, j, s]  = log(sum_i exp(score_i))     (natural log, scaled scores)
- * with score_i = softmax_scale * (q_cat[b, s, :] . [c_i, k_R,i]).  An empty
- * split writes o_part = 0 and lse_part = -inf.
+ * For each part p, each sequence b it touches (rows R = the part's blocks of
+ * b, clipped to L_b) and each head s:
+ *   o_part[p + b, s, :] = sum_{i in R} p_i c_i / sum_{i in R} p_i
+ *   lse_part[p + b, s]  = log(sum_{i in R} exp(score_i))   (natural log)
+ * with score_i = softmax_scale * (q_cat[b, s, :] . [c_i, k_R,i]) and
+ * p_i = exp(score_i).
  *
  *   q_cat      [B, h, d_c + d_r]: q_dtype (MLA_F32 or MLA_BF16)
  *   kv         cache descriptor (host pointer to the struct; its data pointers
  *              are device pointers)
  *   block_table[B, max_blocks_per_seq] int32: physical block of each logical block
- *   seq_lens   [B] int32, each in [1, max_blocks_per_seq * block_size]
- *   o_part     [B, num_splits, h, d_c] float32 (output)
- *   lse_part   [B, num_splits, h] float32 (output)
+ *   seq_lens   [B] int32, each in [1, max_blocks_per_seq * block_size]; a longer
+ *              length is clamped and reported (MLA_DEV_BAD_LENGTH)
+ *   num_parts  1 .. MLA_MAX_PARTS; the tensor-core kernel runs one CTA pair per
+ *              part (about half the SM count fills the GPU once)
+ *   o_part     [mla_decode_num_partials(B, num_parts), h, d_c] float32 (output)
+ *   lse_part   [mla_decode_num_partials(B, num_parts), h] float32 (output)
  *   dev_status int32 device word, may be NULL (see conventions)
  *   flags      MLA_DECODE_AUTO or MLA_DECODE_FORCE_SIMT
- * Supported dtypes: (q, latent, rope) = (F32, F32, F32) on the SIMT kernel;
- * (BF16, BF16, BF16) and (BF16, FP8E4M3, BF16) on both kernels.  The tensor-core
- * kernel runs for d_c = 512, d_r = 64, block_size = 64, h <= 128.
+ * Supported dtypes: (q, latent, rope) = (F32, F32, F32) and (BF16, FP8E4M3, BF16)
+ * on the SIMT kernel; (BF16, BF16, BF16) on both kernels.  The tensor-core
+ * kernel runs for BF16 caches with d_c = 512, d_r = 64, block_size = 64, h <= 128.
  * softmax_scale <= 0 selects 1/sqrt(d_nope + d_r) with d_nope = 128.
  */
 int mla_decode_fwd(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
                    const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
-                   int B, int h, int num_splits, float softmax_scale, float* o_part,
+                   int B, int h, int num_parts, float softmax_scale, float* o_part,
                    float* lse_part, int32_t* dev_status, unsigned flags, void* stream);
 
 /*
- * mla_combine: merge the split partials of mla_decode_fwd (log-sum-exp
- * weighting; the pages do not split the key range, this is the exact merge
- * of softmax attention over disjoint key ranges):
- *   M = max_j lse_part[b, j, s];  w_j = exp(lse_part[b, j, s] - M)
- *   o_lat[b, s, :] = sum_j w_j o_part[b, j, s, :] / sum_j w_j
+ * mla_combine: merge the partials of mla_decode_fwd (log-sum-exp weighting;
+ * the pages do not split the key range, this is the exact merge of softmax
+ * attention over disjoint key ranges).  For sequence b, with J its partial
+ * slots (the parts that touch it, recomputed from seq_lens, block_size,
+ * max_blocks_per_seq and num_parts, which must be those of the decode call):
+ *   M = max_{j in J} lse_part[j, s];  w_j = exp(lse_part[j, s] - M)
+ *   o_lat[b, s, :] = sum_j w_j o_part[j, s, :] / sum_j w_j
  *   lse[b, s]      = M + log(sum_j w_j)
- * Splits with lse = -inf get weight 0; if all are empty, o_lat = 0 and
- * lse = -inf.
- *   o_part [B, num_splits, h, d_c] f32, lse_part [B, num_splits, h] f32
+ * A sequence with no rows gets o_lat = 0 and lse = -inf.
+ *   o_part, lse_part as written by mla_decode_fwd (float32)
  *   o_lat  [B, h, d_c]: o_dtype (MLA_F32 or MLA_BF16) (output)
  *   lse    [B, h] f32 (output, may be NULL)
  * Supported: d_c % 4 == 0, d_c <= 2048.
  */
-int mla_combine(const float* o_part, const float* lse_part, int B, int h, int d_c,
-                int num_splits, void* o_lat, int o_dtype, float* lse, void* stream);
+int mla_combine(const float* o_part, const float* lse_part, const int32_t* seq_lens,
+                int block_size, int max_blocks_per_seq, int B, int h, int d_c, int num_parts,
+                void* o_lat, int o_dtype, float* lse, void* stream);
 
 /*
  * mla_out_proj: W_UV applied after attention (kexue.fm section "Part 1": W_v

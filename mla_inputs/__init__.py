@@ -100,7 +100,6 @@ class Workload:
     dtype: str          # query / weight / rope-key storage: "f32" or "bf16"
     latent_dtype: str   # "f32", "bf16" or "fp8e4m3"
     layout: str         # "contiguous" (identity block table) or "paged" (permuted)
-    num_splits: int     # split-KV chunks per sequence used for the decode step
     d_c: int = 512
     d_r: int = 64
     d_nope: int = 128
@@ -121,15 +120,15 @@ WORKLOADS: dict[str, Workload] = {
     w.name: w
     for w in [
         Workload("tiny_fp32_b1_h16_l512", 1, B=1, h=16, L=512, L_range=None,
-                 dtype="f32", latent_dtype="f32", layout="contiguous", num_splits=4),
+                 dtype="f32", latent_dtype="f32", layout="contiguous"),
         Workload("small_bf16_b64_h16_l4096", 2, B=64, h=16, L=4096, L_range=None,
-                 dtype="bf16", latent_dtype="bf16", layout="contiguous", num_splits=2),
+                 dtype="bf16", latent_dtype="bf16", layout="contiguous"),
         Workload("v3_bf16_b64_h128_l8192", 3, B=64, h=128, L=8192, L_range=None,
-                 dtype="bf16", latent_dtype="bf16", layout="contiguous", num_splits=2),
+                 dtype="bf16", latent_dtype="bf16", layout="contiguous"),
         Workload("paged_bf16_b128_h128_lvar", 4, B=128, h=128, L=None, L_range=(1024, 32768),
-                 dtype="bf16", latent_dtype="bf16", layout="paged", num_splits=4),
+                 dtype="bf16", latent_dtype="bf16", layout="paged"),
         Workload("longctx_fp8_b4_h128_l131072", 5, B=4, h=128, L=131072, L_range=None,
-                 dtype="bf16", latent_dtype="fp8e4m3", layout="contiguous", num_splits=64),
+                 dtype="bf16", latent_dtype="fp8e4m3", layout="contiguous"),
     ]
 }
 

@@ -20,6 +20,8 @@ from .binding import (  # noqa: F401
     mla_cache_fill,
     mla_combine,
     mla_decode_fwd,
+    mla_decode_num_partials,
+    default_num_parts,
     mla_out_proj,
     mla_paged_gather,
     mla_status_string,

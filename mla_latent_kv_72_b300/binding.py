@@ -23,7 +23,8 @@ _LIB = None
 
 EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_version", "mla_cache_bytes_per_token", "mla_absorb_q",
-    "mla_decode_fwd", "mla_combine", "mla_out_proj", "mla_cache_fill", "mla_paged_gather",
+    "mla_decode_num_partials", "mla_decode_fwd", "mla_combine", "mla_out_proj",
+    "mla_cache_fill", "mla_paged_gather",
 )
 
 
@@ -95,8 +96,9 @@ def lib() -> ctypes.CDLL:
         "mla_version": (i32, []),
         "mla_cache_bytes_per_token": (f64, [i32, i32, i32, i32, i32]),
         "mla_absorb_q": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f64, vp]),
+        "mla_decode_num_partials": (i32, [i32, i32]),
         "mla_decode_fwd": (i32, [vp, i32, kvp, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp, u32, vp]),
-        "mla_combine": (i32, [vp, vp, i32, i32, i32, i32, vp, i32, vp, vp]),
+        "mla_combine": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp]),
         "mla_out_proj": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
         "mla_cache_fill": (i32, [vp, vp, i32, vp, i32, i32, vp, i32, kvp, f64, vp, vp]),
         "mla_paged_gather": (i32, [kvp, vp, i32, vp, i32, i32, vp, vp, vp, vp]),
@@ -158,23 +160,38 @@ def mla_absorb_q(q_nope, q_rope, q_pos, w_uk, q_cat, rope_theta=10000.0, stream=
     return q_cat
 
 
-def mla_decode_fwd(q_cat, kv: KVCache, block_table, seq_lens, o_part, lse_part, *,
+def mla_decode_num_partials(B: int, num_parts: int) -> int:
+    n = lib().mla_decode_num_partials(B, num_parts)
+    if n < 0:
+        raise MLAError("mla_decode_num_partials", n)
+    return n
+
+
+def default_num_parts(device=None) -> int:
+    """One part per CTA pair of the device (half its SM count)."""
+    props = torch.cuda.get_device_properties(device if device is not None else torch.cuda.current_device())
+    return max(1, props.multi_processor_count // 2)
+
+
+def mla_decode_fwd(q_cat, kv: KVCache, block_table, seq_lens, num_parts, o_part, lse_part, *,
                    softmax_scale=0.0, dev_status=None, flags=MLA_DECODE_AUTO, stream=None):
-    """Split-KV partials o_part [B, S, h, d_c], lse_part [B, S, h] (see mla72.h)."""
+    """Partials o_part [B + num_parts - 1, h, d_c], lse_part [B + num_parts - 1, h]
+    over the balanced part partition of the block stream (see mla72.h)."""
     B, h, _ = q_cat.shape
-    num_splits = o_part.shape[1]
     _check("mla_decode_fwd", lib().mla_decode_fwd(
         _ptr(q_cat), dtype_code(q_cat.dtype), ctypes.byref(kv), _ptr(block_table),
-        block_table.shape[1], _ptr(seq_lens), B, h, num_splits, float(softmax_scale),
+        block_table.shape[1], _ptr(seq_lens), B, h, int(num_parts), float(softmax_scale),
         _ptr(o_part), _ptr(lse_part), _ptr(dev_status), int(flags), _stream(stream)))
 
 
-def mla_combine(o_part, lse_part, o_lat, lse=None, stream=None):
-    """o_lat [B, h, d_c], lse [B, h] from the split partials (see mla72.h)."""
-    B, S, h, d_c = o_part.shape
+def mla_combine(o_part, lse_part, seq_lens, block_size, max_blocks_per_seq, num_parts, o_lat,
+                lse=None, stream=None):
+    """o_lat [B, h, d_c], lse [B, h] from the partials of mla_decode_fwd (see mla72.h)."""
+    B, h, d_c = o_lat.shape
     _check("mla_combine", lib().mla_combine(
-        _ptr(o_part), _ptr(lse_part), B, h, d_c, S, _ptr(o_lat), dtype_code(o_lat.dtype),
-        _ptr(lse), _stream(stream)))
+        _ptr(o_part), _ptr(lse_part), _ptr(seq_lens), int(block_size), int(max_blocks_per_seq),
+        B, h, d_c, int(num_parts), _ptr(o_lat), dtype_code(o_lat.dtype), _ptr(lse),
+        _stream(stream)))
     return o_lat
 
 

@@ -77,45 +77,57 @@ int mla_absorb_q(const void* q_nope, const void* q_rope, const int32_t* q_pos, c
     return MLA_ERR_SHAPE;
   if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(q_cat))
     return MLA_ERR_ALIGN;
+  if (dtype == MLA_BF16 && d_nope == 128 && d_c == 512 && d_r == 64 && mla::tc_device())
+    return from_cuda(mla::launch_absorb_q_tc(q_nope, q_rope, q_pos, w_uk, q_cat, B, h, rope_theta,
+                                             static_cast<cudaStream_t>(stream)));
   return from_cuda(mla::launch_absorb_q_simt(q_nope, q_rope, q_pos, w_uk, q_cat, B, h, d_nope,
                                              d_c, d_r, dtype, rope_theta,
                                              static_cast<cudaStream_t>(stream)));
 }
 
+int mla_decode_num_partials(int B, int num_parts) {
+  if (B <= 0 || num_parts <= 0 || num_parts > MLA_MAX_PARTS) return MLA_ERR_ARG;
+  return B + num_parts - 1;
+}
+
 int mla_decode_fwd(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
                    const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
-                   int B, int h, int num_splits, float softmax_scale, float* o_part,
+                   int B, int h, int num_parts, float softmax_scale, float* o_part,
                    float* lse_part, int32_t* dev_status, unsigned flags, void* stream) {
   if (!q_cat || !block_table || !seq_lens || !o_part || !lse_part) return MLA_ERR_ARG;
-  if (B <= 0 || h <= 0 || num_splits <= 0 || max_blocks_per_seq <= 0) return MLA_ERR_ARG;
+  if (B <= 0 || h <= 0 || num_parts <= 0 || max_blocks_per_seq <= 0) return MLA_ERR_ARG;
   if (flags > MLA_DECODE_FORCE_SIMT) return MLA_ERR_ARG;
   int st = check_cache(kv);
   if (st != MLA_OK) return st;
   if (!is_float_dtype(q_dtype)) return MLA_ERR_DTYPE;
   if (q_dtype == MLA_F32 && kv->latent_dtype != MLA_F32) return MLA_ERR_DTYPE;
   if (q_dtype == MLA_BF16 && kv->latent_dtype == MLA_F32) return MLA_ERR_DTYPE;
-  if (num_splits > 1024) return MLA_ERR_SHAPE;
+  if (num_parts > MLA_MAX_PARTS) return MLA_ERR_SHAPE;
   if (!aligned16(q_cat) || !aligned16(o_part)) return MLA_ERR_ALIGN;
   float scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / sqrt(128.0 + kv->d_r));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (flags != MLA_DECODE_FORCE_SIMT && mla::decode_tc_supported(q_dtype, *kv, h)) {
     return from_cuda(mla::launch_decode_tc(q_cat, *kv, block_table, max_blocks_per_seq, seq_lens,
-                                           B, h, num_splits, scale, o_part, lse_part, dev_status,
+                                           B, h, num_parts, scale, o_part, lse_part, dev_status,
                                            s));
   }
   return from_cuda(mla::launch_decode_simt(q_cat, q_dtype, *kv, block_table, max_blocks_per_seq,
-                                           seq_lens, B, h, num_splits, scale, o_part, lse_part,
+                                           seq_lens, B, h, num_parts, scale, o_part, lse_part,
                                            dev_status, s));
 }
 
-int mla_combine(const float* o_part, const float* lse_part, int B, int h, int d_c,
-                int num_splits, void* o_lat, int o_dtype, float* lse, void* stream) {
-  if (!o_part || !lse_part || !o_lat) return MLA_ERR_ARG;
-  if (B <= 0 || h <= 0 || d_c <= 0 || num_splits <= 0) return MLA_ERR_ARG;
+int mla_combine(const float* o_part, const float* lse_part, const int32_t* seq_lens,
+                int block_size, int max_blocks_per_seq, int B, int h, int d_c, int num_parts,
+                void* o_lat, int o_dtype, float* lse, void* stream) {
+  if (!o_part || !lse_part || !o_lat || !seq_lens) return MLA_ERR_ARG;
+  if (B <= 0 || h <= 0 || d_c <= 0 || num_parts <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0)
+    return MLA_ERR_ARG;
   if (!is_float_dtype(o_dtype)) return MLA_ERR_DTYPE;
-  if (d_c % 4 != 0 || d_c > 2048 || num_splits > 1024) return MLA_ERR_SHAPE;
+  if (d_c % 4 != 0 || d_c > 2048 || num_parts > MLA_MAX_PARTS) return MLA_ERR_SHAPE;
   if (!aligned16(o_part) || !aligned16(o_lat)) return MLA_ERR_ALIGN;
-  return from_cuda(mla::launch_combine(o_part, lse_part, B, h, d_c, num_splits, o_lat, o_dtype,
+  return from_cuda(mla::launch_combine(o_part, lse_part, seq_lens, block_size,
+                                       max_blocks_per_seq, B, h, d_c, num_parts, o_lat, o_dtype,
                                        lse, static_cast<cudaStream_t>(stream)));
 }
 
@@ -126,6 +138,9 @@ int mla_out_proj(const void* o_lat, const void* w_uv, void* out, int B, int h, i
   if (!is_float_dtype(in_dtype) || !is_float_dtype(out_dtype)) return MLA_ERR_DTYPE;
   if (d_c % 64 != 0 || d_c > 1024 || d_v > 1024) return MLA_ERR_SHAPE;
   if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_ALIGN;
+  if (in_dtype == MLA_BF16 && d_c == 512 && d_v == 128 && mla::tc_device())
+    return from_cuda(mla::launch_out_proj_tc(o_lat, w_uv, out, B, h, out_dtype,
+                                             static_cast<cudaStream_t>(stream)));
   return from_cuda(mla::launch_out_proj_simt(o_lat, w_uv, out, B, h, d_c, d_v, in_dtype,
                                              out_dtype, static_cast<cudaStream_t>(stream)));
 }

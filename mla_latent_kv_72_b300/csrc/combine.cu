@@ -1,7 +1,10 @@
 // mla_combine: log-sum-exp merge of the split-KV partials.
 //
 // Exact merge of softmax attention computed over disjoint key ranges: each
-// range's normalised output is weighted by exp(lse_j - max_j lse_j).
+// range's normalised output is weighted by exp(lse_j - max_j lse_j).  The
+// partials of sequence b are the slots p + b of the parts p that touch it
+// (the balanced part partition of the block stream, recomputed here from the
+// sequence lengths exactly as the decode kernels compute it).
 #include <math.h>
 
 #include "common.cuh"
@@ -14,13 +17,33 @@ constexpr int kMaxSplits = 1024;
 
 // grid: (h, B); block: 128 threads, each owning 4 consecutive latent columns per pass.
 __global__ void __launch_bounds__(kThreads)
-combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part, int B, int h,
-               int d_c, int num_splits, void* __restrict__ o_lat, int o_dtype,
+combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+               const int32_t* __restrict__ seq_lens, int bs, int max_blocks, int B, int h,
+               int d_c, int num_parts, void* __restrict__ o_lat, int o_dtype,
                float* __restrict__ lse_out) {
   __shared__ float sw[kMaxSplits];
   __shared__ float s_m, s_inv, s_lse;
+  __shared__ int s_first, s_count;
   const int s = blockIdx.x, b = blockIdx.y;
-  const int64_t lbase = (int64_t)b * num_splits * h + s;   // lse_part[b, j, s] = lbase + j*h
+  if (threadIdx.x < 32) {
+    long long sb = 0;
+    const long long T = warp_stream_scan(seq_lens, B, bs, max_blocks, b, -1, &sb, nullptr, nullptr);
+    const int nb = seq_blocks(seq_lens, b, bs, max_blocks);
+    if (threadIdx.x == 0) {
+      if (nb == 0) {
+        s_first = 0;
+        s_count = 0;
+      } else {
+        const int P = (int)(T < num_parts ? T : num_parts);
+        const int p0 = part_of(T, P, sb), p1 = part_of(T, P, sb + nb - 1);
+        s_first = p0 + b;
+        s_count = p1 - p0 + 1;
+      }
+    }
+  }
+  __syncthreads();
+  const int num_splits = s_count;
+  const int64_t lbase = (int64_t)s_first * h + s;   // lse of split j: lbase + j*h
 
   // maximum over splits
   float m = -INFINITY;
@@ -66,7 +89,7 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
       float w = sw[j];
       if (w == 0.f) continue;
       const float4 v = *reinterpret_cast<const float4*>(
-          o_part + (((int64_t)b * num_splits + j) * h + s) * d_c + c);
+          o_part + (((int64_t)s_first + j) * h + s) * d_c + c);
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);
@@ -88,12 +111,13 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
 
 }  // namespace
 
-cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int h, int d_c,
-                           int num_splits, void* o_lat, int o_dtype, float* lse, cudaStream_t s) {
-  if (num_splits > kMaxSplits) return cudaErrorInvalidValue;
+cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* seq_lens,
+                           int block_size, int max_blocks, int B, int h, int d_c, int num_parts,
+                           void* o_lat, int o_dtype, float* lse, cudaStream_t s) {
+  if (num_parts > kMaxSplits) return cudaErrorInvalidValue;
   dim3 grid(h, B);
-  combine_kernel<<<grid, kThreads, 0, s>>>(o_part, lse_part, B, h, d_c, num_splits, o_lat,
-                                           o_dtype, lse);
+  combine_kernel<<<grid, kThreads, 0, s>>>(o_part, lse_part, seq_lens, block_size, max_blocks, B,
+                                           h, d_c, num_parts, o_lat, o_dtype, lse);
   return cudaGetLastError();
 }
 

@@ -60,14 +60,67 @@ __host__ __device__ __forceinline__ int dtype_bytes(int dt) {
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Logical block range [lo, hi) of split j for a sequence of nb blocks.
-__host__ __device__ __forceinline__ void split_range(int nb, int num_splits, int j, int* lo,
-                                                     int* hi) {
-  int cb = ceil_div(nb, num_splits);
-  int a = j * cb;
-  int e = a + cb;
-  *lo = a < nb ? a : nb;
-  *hi = e < nb ? e : nb;
+// ---------------------------------------------------------------------------
+// work partition of the decode (shared by the decode kernels and the combine)
+// ---------------------------------------------------------------------------
+//
+// The logical blocks of all sequences, in order (sequence 0's blocks, then
+// sequence 1's, ...), form one stream of T blocks.  With P = min(num_parts, T)
+// effective parts, part p covers stream blocks [floor(p T / P), floor((p+1) T / P));
+// every part is non-empty.  A part writes one partial result (o, lse) per
+// sequence it touches, into slot p + b; slots are unique because parts and
+// sequences are both ordered along the stream.
+
+// Blocks of sequence b (its length clamped to [0, max_blocks * bs]).
+__device__ __forceinline__ int seq_blocks(const int32_t* lens, int b, int bs, int max_blocks) {
+  int L = lens[b];
+  L = L < 0 ? 0 : (L > max_blocks * bs ? max_blocks * bs : L);
+  return (L + bs - 1) / bs;
+}
+
+__host__ __device__ __forceinline__ long long part_begin(long long T, int P, int p) {
+  return (long long)p * T / P;
+}
+
+// The part holding stream block g (largest p with part_begin(p) <= g).
+__host__ __device__ __forceinline__ int part_of(long long T, int P, long long g) {
+  return (int)(((g + 1) * (long long)P - 1) / T);
+}
+
+// Warp-cooperative scan over the sequence lengths (all 32 lanes call it with the
+// same arguments).  Returns T; *s_qb = stream index of block 0 of sequence qb
+// (if 0 <= qb < B); *b_qg / *s_bqg = the sequence holding stream block qg and
+// its first stream block (if 0 <= qg < T; *b_qg = -1 otherwise).
+__device__ __forceinline__ long long warp_stream_scan(const int32_t* lens, int B, int bs,
+                                                     int max_blocks, int qb, long long qg,
+                                                     long long* s_qb, int* b_qg,
+                                                     long long* s_bqg) {
+  const int lane = threadIdx.x & 31;
+  long long run = 0, sq = 0, sg = 0;
+  int bg = -1;
+  for (int base = 0; base < B; base += 32) {
+    const int b = base + lane;
+    const int n = b < B ? seq_blocks(lens, b, bs, max_blocks) : 0;
+    int inc = n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += v;
+    }
+    const long long excl = run + inc - n;
+    if (qb >= base && qb < base + 32) sq = __shfl_sync(0xffffffffu, excl, qb - base);
+    const unsigned own = __ballot_sync(0xffffffffu, n > 0 && qg >= excl && qg < excl + n);
+    if (own != 0u && bg < 0) {
+      const int src = __ffs(own) - 1;
+      bg = base + src;
+      sg = __shfl_sync(0xffffffffu, excl, src);
+    }
+    run += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  if (s_qb) *s_qb = sq;
+  if (b_qg) *b_qg = bg;
+  if (s_bqg) *s_bqg = sg;
+  return run;
 }
 
 // ---------------------------------------------------------------------------
@@ -80,18 +133,29 @@ cudaError_t launch_absorb_q_simt(const void* q_nope, const void* q_rope, const i
 
 cudaError_t launch_decode_simt(const void* q_cat, int q_dtype, const mla_kv_cache& kv,
                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
-                               int B, int h, int num_splits, float scale, float* o_part,
+                               int B, int h, int num_parts, float scale, float* o_part,
                                float* lse_part, int32_t* status, cudaStream_t s);
 
 bool decode_tc_supported(int q_dtype, const mla_kv_cache& kv, int h);
 
+// True on an sm_100-family device with the tensor-map encoder available.
+bool tc_device();
+
+cudaError_t launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int32_t* q_pos,
+                               const void* w_uk, void* q_cat, int B, int h, double theta,
+                               cudaStream_t s);
+
+cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, int B, int h,
+                               int out_dtype, cudaStream_t s);
+
 cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
-                             int B, int h, int num_splits, float scale, float* o_part,
+                             int B, int h, int num_parts, float scale, float* o_part,
                              float* lse_part, int32_t* status, cudaStream_t s);
 
-cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int h, int d_c,
-                           int num_splits, void* o_lat, int o_dtype, float* lse, cudaStream_t s);
+cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* seq_lens,
+                           int block_size, int max_blocks, int B, int h, int d_c, int num_parts,
+                           void* o_lat, int o_dtype, float* lse, cudaStream_t s);
 
 cudaError_t launch_out_proj_simt(const void* o_lat, const void* w_uv, void* out, int B, int h,
                                  int d_c, int d_v, int in_dtype, int out_dtype, cudaStream_t s);

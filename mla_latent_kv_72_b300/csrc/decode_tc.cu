@@ -12,20 +12,28 @@
 //
 // Work split.  One float32 accumulator for 128 heads x 512 latent columns
 // fills the whole 512-column tensor memory of an SM, so a pair of CTAs (a
-// cluster of 2) shares each (sequence, split) work item:
+// cluster of 2) shares each piece of work:
 //   CTA r owns output columns [256 r, 256 r + 256) of the latent (O_r in TMEM)
 //   and the matching slice of the 576-d score contraction: CTA 0 the latent
 //   columns 0..255 plus the 64 RoPE columns, CTA 1 the latent columns 256..511.
 //   Each CTA TMA-loads exactly its own columns of every cache block (the pair
-//   reads each byte of the cache once), computes its partial score tile
-//   S_r = Q[:, K_r] K[:, K_r]^T, and the two partial tiles are exchanged
-//   through distributed shared memory; both CTAs then hold the same
-//   S = S_0 + S_1 (float addition commutes, so both run a bit-identical online
-//   softmax) and write the same P, which each multiplies into its own O_r.
+//   reads each byte of the cache once), computes its partial score tile, and
+//   writes it into the peer's shared memory (one release-ordered remote
+//   arrive per warp); both CTAs then hold the same S = S_0 + S_1 (float addition
+//   commutes, so both run a bit-identical online softmax) and write the same
+//   P, which each multiplies into its own O_r.
 //
-// Roles (192 threads): warp 0 issues TMA loads, warp 1 allocates TMEM and
-// issues tcgen05.mma (one elected lane), warps 2..5 (thread = head row)
-// load the query into TMEM, run the online softmax and the epilogue.
+// Schedule.  The grid is persistent: pair p runs part p of the balanced
+// partition of the whole block stream (all sequences' blocks in order, see
+// common.cuh), one segment (the part's blocks of one sequence) after another,
+// and writes one partial (o, lse) per segment into slot p + b.
+//
+// Roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
+// tcgen05.mma (one lane), warps 2..5 and 6..9 are two softmax warpgroups that
+// take alternate tiles (ping-pong), so that the exchange and softmax of one
+// tile overlap those of the next.  The running maximum is handed from one
+// group to the other per tile; O is rescaled only when the maximum grows by
+// more than kTau (log2 units), so P <= 2^kTau in bf16.
 //
 // TMEM columns: O_r [0, 256), S [256, 320), Q_r [320, 320 + 160) as the MMA
 // A operand (bf16 pairs).  Every wait is bounded; on a timeout the kernel
@@ -38,6 +46,9 @@
 #include "tc_ptx.cuh"
 
 namespace mla {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
 namespace {
 
 using namespace tc;
@@ -52,43 +63,51 @@ constexpr int kRecvBytes = 128 * 64 * 4;    // partial S of the peer, float32
 constexpr int kOffStages = 0;
 constexpr int kOffP = kOffStages + kStages * kStageBytes;
 constexpr int kOffRecv = kOffP + 2 * kPBytes;
-constexpr int kOffBar = kOffRecv + kRecvBytes;
-constexpr int kNumBars = 16;
+constexpr int kOffMpub = kOffRecv + 2 * kRecvBytes;     // [2][128] float
+constexpr int kOffLstate = kOffMpub + 2 * 128 * 4;      // [2 seg][2 group][128] float2
+constexpr int kOffBar = kOffLstate + 2 * 2 * 128 * 8;
+constexpr int kNumBars = 24;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16;
+constexpr int kSmemBytes = kOffMisc + 64;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // alignment slack
+static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS = 256;
 constexpr uint32_t kColQ = 320;
 constexpr uint32_t kTmemCols = 512;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kTau = 8.0f;  // lazy rescale threshold (log2 units): P stays <= 2^8
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // barrier indices
 enum {
-  BAR_KV_FULL = 0,   // [kStages]
-  BAR_KV_EMPTY = 3,  // [kStages]
-  BAR_S_FULL = 6,
-  BAR_S_EMPTY = 7,
-  BAR_P_FULL = 8,    // [2]
-  BAR_O_DONE = 10,   // [2]
-  BAR_Q_READY = 12,
-  BAR_RECV_FULL = 13,
-  BAR_RECV_FREE = 14,
-  BAR_DRAIN = 15,
+  BAR_KV_FULL = 0,    // [kStages] TMA -> MMA
+  BAR_KV_EMPTY = 3,   // [kStages] MMA (commit after P.C) -> TMA
+  BAR_S_FULL = 6,     // [2] MMA -> softmax group (k & 1); one barrier per group so that
+                      //     a group's parity waits never alias the other group's phases
+  BAR_S_EMPTY = 8,    // softmax (4 warps) -> MMA
+  BAR_P_FULL = 9,     // [2] softmax (4 warps) -> MMA
+  BAR_O_DONE = 11,    // [2] MMA -> softmax (P buffer free, O final)
+  BAR_RECV_FULL = 13, // [2] peer's 4 warps have written their partial scores here
+  BAR_PEER_FREE = 15, // [2] peer's 4 warps have read what we sent
+  BAR_MREADY = 17,    // [2] running maximum of a tile published (4 warps)
+  BAR_Q_FREE = 19,    // MMA: last score MMA of a segment done
+  BAR_Q_READY = 20,   // softmax (8 warps): query slice of a segment in TMEM
+  BAR_O_FREE = 21,    // softmax (8 warps): O of a segment read out
+  BAR_SEG = 22,       // softmax (8 warps): end-of-segment rendezvous
+  BAR_DRAIN = 23,
 };
 
 struct TcParams {
   const uint16_t* q_cat;        // [B, h, 576] bf16
   const int32_t* block_table;   // [B, max_blocks]
   const int32_t* seq_lens;      // [B]
-  float* o_part;                // [B, S, h, 512]
-  float* lse_part;              // [B, S, h]
+  float* o_part;                // [B + P - 1, h, 512]
+  float* lse_part;              // [B + P - 1, h]
   int32_t* status;
-  int max_blocks, B, h, num_splits, num_blocks;
+  int max_blocks, B, h, num_parts, num_blocks;
   float scale_log2;
   long long wait_limit;
 };
@@ -97,6 +116,37 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+
+// Walks the part's tiles (sequence b, logical block blk) in stream order.
+struct TileIter {
+  const int32_t* lens;
+  int maxb, b, blk, nb;
+  __device__ void init(const int32_t* l, int max_blocks, int b0, int blk0) {
+    lens = l;
+    maxb = max_blocks;
+    b = b0;
+    blk = blk0;
+    nb = seq_blocks(lens, b, kTok, maxb);
+  }
+  // only called while another tile of the part follows, so b stays < B
+  __device__ void next() {
+    if (++blk >= nb) {
+      blk = 0;
+      do {
+        ++b;
+        nb = seq_blocks(lens, b, kTok, maxb);
+      } while (nb == 0);
+    }
+  }
+  __device__ int len() const {
+    int L = lens[b];
+    return L < 0 ? 0 : (L > maxb * kTok ? maxb * kTok : L);
+  }
+  __device__ int valid() const {
+    const int n = len() - blk * kTok;
+    return n < kTok ? n : kTok;
+  }
+};
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
@@ -108,73 +158,103 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int work = blockIdx.x / 2;
-  const int b = work / p.num_splits, j = work % p.num_splits;
+  const int part = blockIdx.x / 2;
 
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8 * i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* info = reinterpret_cast<int*>(smem + kOffMisc + 16);  // b0, blk0, ntiles
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(BAR_KV_FULL + s), 1);
       mbar_init(bar(BAR_KV_EMPTY + s), 1);
     }
-    mbar_init(bar(BAR_S_FULL), 1);
-    mbar_init(bar(BAR_S_EMPTY), 128);
-    mbar_init(bar(BAR_P_FULL + 0), 128);
-    mbar_init(bar(BAR_P_FULL + 1), 128);
-    mbar_init(bar(BAR_O_DONE + 0), 1);
-    mbar_init(bar(BAR_O_DONE + 1), 1);
-    mbar_init(bar(BAR_Q_READY), 128);
-    mbar_init(bar(BAR_RECV_FULL), 128);
-    mbar_init(bar(BAR_RECV_FREE), 128);
+    mbar_init(bar(BAR_S_EMPTY), 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(BAR_S_FULL + i), 1);
+      mbar_init(bar(BAR_P_FULL + i), 4);
+      mbar_init(bar(BAR_O_DONE + i), 1);
+      mbar_init(bar(BAR_RECV_FULL + i), 4);
+      mbar_init(bar(BAR_PEER_FREE + i), 4);
+      mbar_init(bar(BAR_MREADY + i), 4);
+    }
+    mbar_init(bar(BAR_Q_FREE), 1);
+    mbar_init(bar(BAR_Q_READY), 8);
+    mbar_init(bar(BAR_O_FREE), 8);
+    mbar_init(bar(BAR_SEG), 8);
     mbar_init(bar(BAR_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_lat);
-    prefetch_tmap(&tm_rope);
+  if (warp == 0) {
+    // this part's range of the block stream (both CTAs compute the same)
+    const long long T = warp_stream_scan(p.seq_lens, p.B, kTok, p.max_blocks, -1, -1, nullptr,
+                                         nullptr, nullptr);
+    const int P = (int)(T < p.num_parts ? T : p.num_parts);
+    int b0 = -1;
+    long long g0 = 0, g1 = 0, sb = 0;
+    if (part < P) {
+      g0 = part_begin(T, P, part);
+      g1 = part_begin(T, P, part + 1);
+      warp_stream_scan(p.seq_lens, p.B, kTok, p.max_blocks, -1, g0, nullptr, &b0, &sb);
+    }
+    if (lane == 0) {
+      info[0] = b0;
+      info[1] = (int)(g0 - sb);
+      info[2] = (int)(g1 - g0);
+      prefetch_tmap(&tm_lat);
+      prefetch_tmap(&tm_rope);
+      if (part == 0 && rank == 0)
+        for (int b = 0; b < p.B; ++b)
+          if (p.seq_lens[b] > p.max_blocks * kTok) set_status(p.status, MLA_DEV_BAD_LENGTH);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
-  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated, part known
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-
-  int L = p.seq_lens[b];
-  if (L > p.max_blocks * kTok) {
-    if (threadIdx.x == 0 && rank == 0) set_status(p.status, MLA_DEV_BAD_LENGTH);
-    L = p.max_blocks * kTok;
-  }
-  if (L < 0) L = 0;
-  int blo, bhi;
-  split_range(ceil_div(L, kTok), p.num_splits, j, &blo, &bhi);
-  const int T = bhi - blo;
+  const int b_first = info[0], blk_first = info[1], ntiles = info[2];
   const long long lim = p.wait_limit;
+  bool timed_out = false;
 
   auto fail = [&]() {
-    set_status(p.status, MLA_DEV_WAIT_TIMEOUT);
+    if (timed_out) set_status(p.status, MLA_DEV_WAIT_TIMEOUT);
     *abort_flag = 1;
   };
+  // lane 0 waits, the warp learns the result
+  auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_or_abort(b, parity, lim, abort_flag, &timed_out);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  };
+  auto warp_wait_cluster = [&](uint32_t b, uint32_t parity) -> bool {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_or_abort<true>(b, parity, lim, abort_flag, &timed_out);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  };
 
-  if (T > 0 && warp == 0) {
+  if (b_first >= 0 && ntiles > 0 && warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      TileIter it;
+      it.init(p.seq_lens, p.max_blocks, b_first, blk_first);
       const uint32_t tx = rank == 0 ? 5 * kBoxBytes : 4 * kBoxBytes;
-      int issued[kStages] = {0, 0, 0};
-      for (int i = 0; i < T; ++i) {
+      int k = 0;
+      for (; k < ntiles; ++k) {
         if (*abort_flag) break;
-        const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(bar(BAR_KV_EMPTY + st), ((i / kStages) - 1) & 1, lim)) {
+        const int st = k % kStages;
+        if (k >= kStages &&
+            !mbar_wait_or_abort(bar(BAR_KV_EMPTY + st), ((k / kStages) - 1) & 1, lim, abort_flag,
+                                &timed_out)) {
           fail();
           break;
         }
-        int pb = p.block_table[(int64_t)b * p.max_blocks + blo + i];
+        int pb = p.block_table[(int64_t)it.b * p.max_blocks + it.blk];
         if (pb < 0 || pb >= p.num_blocks) {
           set_status(p.status, MLA_DEV_BAD_BLOCK);
           pb = 0;  // load a valid block instead; the result is flagged as wrong
@@ -183,54 +263,61 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         const uint32_t fb = bar(BAR_KV_FULL + st);
         mbar_arrive_expect_tx(fb, tx);
         const int y = pb * kTok;
-        for (int k = 0; k < 4; ++k)
-          tma_load_2d(dst + k * kBoxBytes, &tm_lat, (int)(rank * 4 + k) * 64, y, fb);
+        for (int c = 0; c < 4; ++c)
+          tma_load_2d(dst + c * kBoxBytes, &tm_lat, (int)(rank * 4 + c) * 64, y, fb);
         if (rank == 0) tma_load_2d(dst + 4 * kBoxBytes, &tm_rope, 0, y, fb);
-        issued[st]++;
+        if (k + 1 < ntiles) it.next();
       }
-      // wait for every issued load to land before the CTA may exit
-      for (int st = 0; st < kStages; ++st)
-        if (issued[st] > 0) mbar_wait(bar(BAR_KV_FULL + st), (issued[st] - 1) & 1, lim);
+      // every issued load must land before the CTA may exit
+      bool dummy = false;
+      for (int st = 0; st < kStages; ++st) {
+        const int n = (k - st + kStages - 1) / kStages;  // loads issued into stage st
+        if (n > 0) {
+          int never = 0;
+          mbar_wait_or_abort(bar(BAR_KV_FULL + st), (n - 1) & 1, lim, &never, &dummy);
+        }
+      }
     }
-  } else if (T > 0 && warp == 1) {
+  } else if (b_first >= 0 && ntiles > 0 && warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idS = idesc_bf16_f32(128, 64, false, false);
     const uint32_t idO = idesc_bf16_f32(128, 256, false, true);
     const int nK = rank == 0 ? 20 : 16;     // 16-wide K steps of the partial score
     const int nbox = rank == 0 ? 5 : 4;
-    bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q_READY), 0, lim));
-    if (!ok) fail();
-    tc_fence_after();
+    TileIter it;
+    it.init(p.seq_lens, p.max_blocks, b_first, blk_first);
 
-    auto issue_o = [&](int t) -> bool {
-      bool w = __all_sync(0xffffffffu, mbar_wait(bar(BAR_P_FULL + (t & 1)), (t >> 1) & 1, lim));
-      if (!w) return false;
+    // O += P(j) C(j); the first tile of a segment overwrites O
+    auto issue_o = [&](int j, bool first_j, int seg_j) -> bool {
+      if (first_j && seg_j > 0 && !warp_wait(bar(BAR_O_FREE), (seg_j - 1) & 1)) return false;
+      if (!warp_wait(bar(BAR_P_FULL + (j & 1)), (j >> 1) & 1)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t stage = sbase + kOffStages + (t % kStages) * kStageBytes;
-        const uint32_t pbuf = sbase + kOffP + (t & 1) * kPBytes;
+        const uint32_t stage = sbase + kOffStages + (j % kStages) * kStageBytes;
+        const uint32_t pbuf = sbase + kOffP + (j & 1) * kPBytes;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t ad = smem_desc(pbuf + k * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(stage + k * 2048, kBoxBytes, 1024, kSwizzle128B);
-          mma_ss(tmem + kColO, ad, bd, idO, (t > 0 || k > 0) ? 1u : 0u);
+        for (int c = 0; c < 4; ++c) {
+          const uint64_t ad = smem_desc(pbuf + c * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(stage + c * 2048, kBoxBytes, 1024, kSwizzle128B);
+          mma_ss(tmem + kColO, ad, bd, idO, (first_j && c == 0) ? 0u : 1u);
         }
-        mma_commit(bar(BAR_O_DONE + (t & 1)));
-        mma_commit(bar(BAR_KV_EMPTY + (t % kStages)));
+        mma_commit(bar(BAR_O_DONE + (j & 1)));
+        mma_commit(bar(BAR_KV_EMPTY + (j % kStages)));
       }
       __syncwarp();
       return true;
     };
 
-    for (int i = 0; i < T && ok; ++i) {
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
-      const int st = i % kStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KV_FULL + st), (i / kStages) & 1, lim))) {
-        ok = false;
-        break;
-      }
-      const uint32_t stage = sbase + kOffStages + st * kStageBytes;
-      const int n_valid = min(kTok, L - (blo + i) * kTok);
+    bool ok = true;
+    int seg = 0, prev_seg = 0;
+    bool prev_first = false;
+    for (int k = 0; k < ntiles; ++k) {
+      const bool first = (k == 0) || (it.blk == 0);
+      const bool last = (k == ntiles - 1) || (it.blk == it.nb - 1);
+      const int st = k % kStages;
+      if (first && !warp_wait(bar(BAR_Q_READY), seg & 1)) { ok = false; break; }
+      if (!warp_wait(bar(BAR_KV_FULL + st), (k / kStages) & 1)) { ok = false; break; }
+      const int n_valid = it.valid();
       if (n_valid < kTok) {
         // slots past the sequence end: zero them so that P = 0 meets finite values
         uint8_t* sp = smem + kOffStages + st * kStageBytes;
@@ -243,80 +330,94 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (i > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait(bar(BAR_S_EMPTY), (i - 1) & 1, lim))) {
-        ok = false;
-        break;
-      }
+      if (k > 0 && !warp_wait(bar(BAR_S_EMPTY), (k - 1) & 1)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
-        for (int k = 0; k < nK; ++k) {
-          const uint64_t bd = smem_desc(stage + (k >> 2) * kBoxBytes + (k & 3) * 32, 16, 1024,
+        const uint32_t stage = sbase + kOffStages + st * kStageBytes;
+        for (int kk = 0; kk < nK; ++kk) {
+          const uint64_t bd = smem_desc(stage + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024,
                                         kSwizzle128B);
-          mma_ts(tmem + kColS, tmem + kColQ + 8 * k, bd, idS, k > 0 ? 1u : 0u);
+          mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bd, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(BAR_S_FULL));
+        mma_commit(bar(BAR_S_FULL + (k & 1)));
+        if (last) mma_commit(bar(BAR_Q_FREE));
       }
       __syncwarp();
-      if (i > 0 && !issue_o(i - 1)) { ok = false; break; }
+      if (k > 0 && !issue_o(k - 1, prev_first, prev_seg)) { ok = false; break; }
+      prev_first = first;
+      prev_seg = seg;
+      if (last) ++seg;
+      if (k + 1 < ntiles) it.next();
     }
-    if (ok && !__any_sync(0xffffffffu, *abort_flag != 0)) ok = issue_o(T - 1);
+    if (ok) ok = issue_o(ntiles - 1, prev_first, prev_seg);
     if (!ok) fail();
     // drain: every MMA issued by this thread has completed
-    if (lane == 0) mma_commit(bar(BAR_DRAIN));
+    if (lane == 0) {
+      mma_commit(bar(BAR_DRAIN));
+      int never = 0;
+      bool dummy = false;
+      mbar_wait_or_abort(bar(BAR_DRAIN), 0, lim, &never, &dummy);
+    }
     __syncwarp();
-    mbar_wait(bar(BAR_DRAIN), 0, lim);
-  } else if (warp >= 2) {
-    // ------------------------------------------------------------ softmax / epilogue
+  } else if (b_first >= 0 && ntiles > 0 && warp >= 2) {
+    // ------------------------------------------------------------ softmax groups
+    const int g = (warp - 2) >> 2;            // group: tiles k with (k & 1) == g
     const int sub = warp & 3;                 // TMEM sub-partition of this warp
     const int row = sub * 32 + lane;          // head
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
     const bool live = row < p.h;
-    float* orow = p.o_part + (((int64_t)b * p.num_splits + j) * p.h + row) * 512 + rank * 256;
+    const bool group_lead = (warp == 2 + 4 * g) && lane == 0;
+    const int sw16 = row & 15, sw8 = row & 7;
+    float* mpub = reinterpret_cast<float*>(smem + kOffMpub);
+    float2* lstate = reinterpret_cast<float2*>(smem + kOffLstate);
+    const uint32_t my_recv_u32 = sbase + kOffRecv + g * kRecvBytes + row * 256;
+    const uint8_t* my_recv = smem + kOffRecv + g * kRecvBytes + row * 256;
+    const uint32_t peer_recv = mapa(my_recv_u32, peer);
+    const uint32_t peer_recv_full = mapa(bar(BAR_RECV_FULL + g), peer);
+    const uint32_t peer_free = mapa(bar(BAR_PEER_FREE + g), peer);
 
-    if (T == 0) {
-      if (live) {
-        for (int c = 0; c < 256; c += 4)
-          *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (rank == 0) p.lse_part[((int64_t)b * p.num_splits + j) * p.h + row] = -INFINITY;
-      }
-    } else {
-      // query slice -> TMEM (A operand): CTA 0 dims [0,256) ++ [512,576), CTA 1 dims [256,512)
-      {
-        const uint4* q = reinterpret_cast<const uint4*>(p.q_cat + ((int64_t)b * p.h + (live ? row : 0)) * 576);
-        const int nq = rank == 0 ? 160 : 128;
-        for (int c0 = 0; c0 < nq; c0 += 16) {
-          uint32_t w[16];
+    // query slice of sequence b -> TMEM (A operand).  CTA 0 holds dims
+    // [0, 256) ++ [512, 576), CTA 1 dims [256, 512); 16-column chunks (32
+    // dims) are split between the two groups.
+    auto load_q = [&](int b) {
+      const uint4* q = reinterpret_cast<const uint4*>(p.q_cat + ((int64_t)b * p.h + (live ? row : 0)) * 576);
+      const int nchunk = rank == 0 ? 10 : 8;
+      const int c0 = g * (nchunk / 2), c1 = c0 + nchunk / 2;
+      for (int c = c0; c < c1; ++c) {
+        const int dim0 = rank == 0 ? (c < 8 ? 32 * c : 512 + 32 * (c - 8)) : 256 + 32 * c;
+        uint32_t w[16];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int g = c0 / 4 + u;  // 8-dim group index within this CTA's slice
-            const int gsrc = rank == 0 ? (g < 32 ? g : 64 + (g - 32)) : 32 + g;
-            uint4 v = live ? q[gsrc] : make_uint4(0, 0, 0, 0);
-            w[4 * u + 0] = v.x;
-            w[4 * u + 1] = v.y;
-            w[4 * u + 2] = v.z;
-            w[4 * u + 3] = v.w;
-          }
-          tmem_st16(tl + kColQ + c0, w);
+        for (int u = 0; u < 4; ++u) {
+          const uint4 v = live ? q[dim0 / 8 + u] : make_uint4(0, 0, 0, 0);
+          w[4 * u + 0] = v.x;
+          w[4 * u + 1] = v.y;
+          w[4 * u + 2] = v.z;
+          w[4 * u + 3] = v.w;
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(BAR_Q_READY));
+        tmem_st16(tl + kColQ + 16 * c, w);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_Q_READY));
+    };
 
-      const uint32_t peer_recv = mapa(sbase + kOffRecv + row * 256, peer);
-      const uint32_t peer_recv_full = mapa(bar(BAR_RECV_FULL), peer);
-      const uint32_t peer_recv_free = mapa(bar(BAR_RECV_FREE), peer);
-      const uint8_t* my_recv = smem + kOffRecv + row * 256;
-      const int sw16 = row & 15, sw8 = row & 7;
+    TileIter it;
+    it.init(p.seq_lens, p.max_blocks, b_first, blk_first);
+    float m_g = -INFINITY, l_g = 0.f;   // running max / sum of this group's tiles
+    int seg = 0;
+    bool ok = true;
+    load_q(it.b);
 
-      float m_run = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int i = 0; i < T; ++i) {
-        if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
-        const int n_valid = min(kTok, L - (blo + i) * kTok);
-        // partial scores of this CTA
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_S_FULL), i & 1, lim))) { ok = false; break; }
+    for (int k = 0; k < ntiles && ok; ++k) {
+      const bool first = (k == 0) || (it.blk == 0);
+      const bool last = (k == ntiles - 1) || (it.blk == it.nb - 1);
+
+      if ((k & 1) == g) {
+        const int u = k >> 1;  // use index of this group's exchange buffers
+        const int n_valid = it.valid();
+        // ---- partial scores of this CTA
+        if (!warp_wait(bar(BAR_S_FULL + g), u & 1)) { ok = false; break; }
         tc_fence_after();
         uint32_t r[64];
         tmem_ld16(tl + kColS + 0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
@@ -325,57 +426,72 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         tmem_ld16(tl + kColS + 48, *reinterpret_cast<uint32_t(*)[16]>(&r[48]));
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar(BAR_S_EMPTY));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_S_EMPTY));
 
-        // exchange partial scores with the peer CTA
-        if (i > 0 && !__all_sync(0xffffffffu, mbar_wait<true>(bar(BAR_RECV_FREE), (i - 1) & 1, lim))) {
-          ok = false;
-          break;
-        }
+        // ---- exchange with the peer CTA
+        if (u >= 1 && !warp_wait_cluster(bar(BAR_PEER_FREE + g), (u - 1) & 1)) { ok = false; break; }
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           st_cluster_v4(peer_recv + ((c ^ sw16) << 4), __uint_as_float(r[4 * c]),
                         __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
                         __uint_as_float(r[4 * c + 3]));
-        mbar_arrive_remote(peer_recv_full);
-        if (!__all_sync(0xffffffffu, mbar_wait<true>(bar(BAR_RECV_FULL), i & 1, lim))) {
-          ok = false;
-          break;
-        }
-        float x[64];
+        // one release arrive per warp publishes the warp's 32 rows to the peer
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(peer_recv_full);
+        if (!warp_wait_cluster(bar(BAR_RECV_FULL + g), u & 1)) { ok = false; break; }
+        // full score (log2 domain) in place: r <- (own partial + peer's) * scale
+        float mt = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const float4 v = *reinterpret_cast<const float4*>(my_recv + ((c ^ sw16) << 4));
-          x[4 * c + 0] = __uint_as_float(r[4 * c + 0]) + v.x;
-          x[4 * c + 1] = __uint_as_float(r[4 * c + 1]) + v.y;
-          x[4 * c + 2] = __uint_as_float(r[4 * c + 2]) + v.z;
-          x[4 * c + 3] = __uint_as_float(r[4 * c + 3]) + v.w;
-        }
-        mbar_arrive_remote(peer_recv_free);
-
-        // online softmax (log2 domain) with lazy rescaling of O
-        float mt = -INFINITY;
+          const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          x[k] = k < n_valid ? x[k] * p.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[k]);
-        }
-        bool need = false;
-        float m_new = m_run;
-        if (i == 0) {
-          m_run = mt;
-        } else if (mt > m_run + kTau) {
-          need = true;
-          m_new = mt;
-        }
-        if (__any_sync(0xffffffffu, need)) {
-          const int t = i - 1;
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_O_DONE + (t & 1)), (t >> 1) & 1, lim))) {
-            ok = false;
-            break;
+          for (int e = 0; e < 4; ++e) {
+            const int kk = 4 * c + e;
+            const float xs = kk < n_valid ? (__uint_as_float(r[kk]) + vv[e]) * p.scale_log2
+                                          : -INFINITY;
+            r[kk] = __float_as_uint(xs);
+            mt = fmaxf(mt, xs);
           }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(peer_free);
+
+        // ---- running maximum, handed over from the previous tile's group
+        float m_prev = -INFINITY;
+        if (!first) {
+          const int kp = k - 1;
+          if (!warp_wait(bar(BAR_MREADY + (kp & 1)), (kp >> 1) & 1)) { ok = false; break; }
+          m_prev = mpub[(kp & 1) * 128 + row];
+        }
+        float m_k = m_prev;
+        bool resc = false;
+        if (m_prev == -INFINITY) {
+          m_k = mt;
+        } else if (mt > m_prev + kTau) {
+          m_k = mt;
+          resc = true;
+        }
+        mpub[(k & 1) * 128 + row] = m_k;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_MREADY + (k & 1)));
+        if (m_g != m_k) {
+          if (m_g != -INFINITY) l_g *= exp2f(m_g - m_k);
+          m_g = m_k;
+        }
+
+        // ---- P buffer (k & 1) was last read by the P.C MMA of tile k-2; waiting
+        // for it first also means O(k-3) is done, so the wait on the other
+        // group's O_DONE below cannot alias an older phase
+        if (k >= 2 && !warp_wait(bar(BAR_O_DONE + (k & 1)), ((k - 2) >> 1) & 1)) { ok = false; break; }
+
+        // ---- rescale O between P(k-1) C and P(k) C (rare)
+        if (__any_sync(0xffffffffu, resc)) {
+          const int kp = k - 1;
+          if (!warp_wait(bar(BAR_O_DONE + (kp & 1)), (kp >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          const float alpha = need ? exp2f(m_run - m_new) : 1.0f;
+          const float alpha = resc ? exp2f(m_prev - m_k) : 1.0f;
           for (int c = 0; c < 16; ++c) {
             uint32_t v[16];
             tmem_ld16(tl + kColO + 16 * c, v);
@@ -385,63 +501,80 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             tmem_st16(tl + kColO + 16 * c, v);
           }
           tmem_wait_st();
-          l *= alpha;
-          m_run = m_new;
         }
 
-        // P (bf16) for this tile; its buffer was last read by the O MMA of tile i-2
-        if (i >= 2 &&
-            !__all_sync(0xffffffffu, mbar_wait(bar(BAR_O_DONE + (i & 1)), ((i - 2) >> 1) & 1, lim))) {
-          ok = false;
-          break;
-        }
-        uint8_t* prow = smem + kOffP + (i & 1) * kPBytes + row * 128;
+        // ---- P (bf16)
+        uint8_t* prow = smem + kOffP + (k & 1) * kPBytes + row * 128;
         float psum = 0.f;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t pk[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float p0 = exp2f(x[8 * c + 2 * e] - m_run);
-            const float p1 = exp2f(x[8 * c + 2 * e + 1] - m_run);
+            const float p0 = exp2f(__uint_as_float(r[8 * c + 2 * e]) - m_k);
+            const float p1 = exp2f(__uint_as_float(r[8 * c + 2 * e + 1]) - m_k);
             psum += p0 + p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
           *reinterpret_cast<uint4*>(prow + ((c ^ sw8) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        l += psum;
+        l_g += psum;
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(BAR_P_FULL + (i & 1)));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_P_FULL + (k & 1)));
       }
 
-      if (!ok) fail();
-      // epilogue: O_r / l -> o_part, lse (CTA 0)
-      if (ok && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-        const int t = T - 1;
-        const bool w = __all_sync(0xffffffffu, mbar_wait(bar(BAR_O_DONE + (t & 1)), (t >> 1) & 1, lim));
-        if (!w) {
-          fail();
-        } else {
+      if (last) {
+        // ---- end of a segment: both groups
+        float2* ls = lstate + (seg & 1) * 256;
+        ls[g * 128 + row] = make_float2(m_g, l_g);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_SEG));
+        if (!warp_wait(bar(BAR_SEG), seg & 1)) { ok = false; break; }
+        const float2 o = ls[(1 - g) * 128 + row];
+        const float M = fmaxf(m_g, o.x);
+        const float l = (m_g != -INFINITY ? l_g * exp2f(m_g - M) : 0.f) +
+                        (o.x != -INFINITY ? o.y * exp2f(o.x - M) : 0.f);
+        const int b = it.b;
+        // query of the next segment first: the MMA warp issues the last P.C
+        // of this segment only after the next segment's first score MMA
+        if (k + 1 < ntiles) {
+          TileIter nx = it;
+          nx.next();
+          if (!warp_wait(bar(BAR_Q_FREE), seg & 1)) { ok = false; break; }
           tc_fence_after();
-          const float inv = 1.0f / l;
-          for (int c = 0; c < 16; ++c) {
-            uint32_t v[16];
-            tmem_ld16(tl + kColO + 16 * c, v);
-            tmem_wait_ld();
-            if (live) {
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<float4*>(orow + 16 * c + 4 * q4) =
-                    make_float4(__uint_as_float(v[4 * q4]) * inv, __uint_as_float(v[4 * q4 + 1]) * inv,
-                                __uint_as_float(v[4 * q4 + 2]) * inv, __uint_as_float(v[4 * q4 + 3]) * inv);
-            }
-          }
-          if (live && rank == 0)
-            p.lse_part[((int64_t)b * p.num_splits + j) * p.h + row] = (m_run + log2f(l)) * kLn2;
+          load_q(nx.b);
         }
+        // epilogue: O_r / l -> o_part slot (part + b); this group's 128 columns
+        if (!warp_wait(bar(BAR_O_DONE + (k & 1)), (k >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const int64_t slot = (int64_t)part + b;
+        float* orow = p.o_part + (slot * p.h + row) * 512 + rank * 256 + g * 128;
+        const float inv = 1.0f / l;
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[16];
+          tmem_ld16(tl + kColO + g * 128 + 16 * c, v);
+          tmem_wait_ld();
+          if (live) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              *reinterpret_cast<float4*>(orow + 16 * c + 4 * q4) =
+                  make_float4(__uint_as_float(v[4 * q4]) * inv, __uint_as_float(v[4 * q4 + 1]) * inv,
+                              __uint_as_float(v[4 * q4 + 2]) * inv, __uint_as_float(v[4 * q4 + 3]) * inv);
+          }
+        }
+        if (live && rank == 0 && g == 0) p.lse_part[slot * p.h + row] = (M + log2f(l)) * kLn2;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_O_FREE));
+        m_g = -INFINITY;
+        l_g = 0.f;
+        ++seg;
       }
+      if (k + 1 < ntiles) it.next();
     }
+    if (!ok) fail();
   }
 
   // teardown: TMEM free after every reader is done; the cluster stays up until
@@ -459,20 +592,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 // host side
 // ---------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() { return tensor_map_encoder(); }
 
 // 2-D bf16 view [rows, cols] with the given row pitch, 64 x 64 boxes, 128-byte swizzle.
 bool make_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
@@ -504,15 +624,32 @@ int device_major() {
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool tc_device() { return device_major() >= 10 && get_encode_fn() != nullptr; }
+
 bool decode_tc_supported(int q_dtype, const mla_kv_cache& kv, int h) {
   return q_dtype == MLA_BF16 && kv.latent_dtype == MLA_BF16 && kv.rope_dtype == MLA_BF16 &&
          kv.d_c == 512 && kv.d_r == 64 && kv.block_size == kTok && h >= 1 && h <= 128 &&
-         device_major() >= 10 && get_encode_fn() != nullptr;
+         tc_device();
 }
 
 cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
-                             int B, int h, int num_splits, float scale, float* o_part,
+                             int B, int h, int num_parts, float scale, float* o_part,
                              float* lse_part, int32_t* status, cudaStream_t s) {
   CUtensorMap tm_lat, tm_rope;
   const uint64_t rows = (uint64_t)kv.num_blocks * kv.block_size;
@@ -536,11 +673,11 @@ cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
   prm.max_blocks = max_blocks;
   prm.B = B;
   prm.h = h;
-  prm.num_splits = num_splits;
+  prm.num_parts = num_parts;
   prm.num_blocks = kv.num_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.wait_limit = 4000000000LL;  // about 2 s of SM clock
-  dim3 grid(2 * B * num_splits);
+  dim3 grid(2 * num_parts);
   decode_tc_kernel<<<grid, kThreads, kSmemAlloc, s>>>(tm_lat, tm_rope, prm);
   return cudaGetLastError();
 }

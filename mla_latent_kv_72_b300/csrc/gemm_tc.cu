@@ -1,0 +1,314 @@
+// Per-head GEMMs of the absorbed decode on the tensor cores (tcgen05 + TMEM +
+// TMA), bf16 in, float32 accumulate:
+//
+//   mla_absorb_q  (kexue.fm "From MHA, MQA, GQA to MLA", section "Part 1" and
+//                  its note 2; eq. mla-mqa, first block of q):
+//     q_cat[b, s, c] = sum_d q_nope[b, s, d] W_UK[s, d, c]   (c < 512), and the
+//     rotary part q_cat[b, s, 512 + j] = RoPE(q_rope[b, s, :], q_pos[b])[j].
+//   mla_out_proj  (eq. mla-mqa, first line: o_t = [o^(s) W_v^(s)]):
+//     out[b, s, v] = sum_c o_lat[b, s, c] W_UV[s, v, c].
+//
+// Both have the form D[m][n] = sum_k A_s[m][k] X_s[n][k] per head s, with m an
+// output feature (the 128 TMEM lanes), n the batch row (TMEM columns, up to
+// 256 per CTA) and k the contraction, streamed in 64-wide chunks by TMA:
+//   absorb:   A_s[c][d] = W_UK[s][d][c]  (MN-major A: c is contiguous),
+//             X_s[b][d] = q_nope[b][s][d] (K-major, a 3-D box over (d, s, b));
+//   out_proj: A_s[v][c] = W_UV[s][v][c]  (K-major A),
+//             X_s[b][c] = o_lat[b][s][c]  (K-major, a 3-D box over (c, s, b)).
+// Grid (h, m tiles, batch tiles); 128 threads: warp 0 issues TMA, warp 1 owns
+// TMEM and issues the MMAs, all four warps run the epilogue (thread = m).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace mla {
+
+// defined in decode_tc.cu
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+namespace {
+
+using namespace tc;
+
+constexpr int kKChunk = 64;                 // contraction elements per stage
+constexpr int kStagesG = 4;
+constexpr int kABytes = 128 * kKChunk * 2;  // 16 KB: 128 m x 64 k
+constexpr int kMaxN = 256;
+constexpr int kGThreads = 128;
+
+struct GemmParams {
+  int K;            // contraction length (multiple of 64)
+  int n_tile;       // batch rows per CTA (multiple of 16, <= 256)
+  int nstage;       // pipeline stages (<= kStagesG)
+  int stage_bytes;  // A chunk + X chunk, multiple of 1024
+  int tmem_cols;    // power of two >= max(32, n_tile)
+  int B, h;
+  void* out;        // element (b, s, m) at out + (b * h + s) * out_ld + m
+  int out_ld;
+  int out_dtype;
+  // rotary part of the absorbed query (absorb only, m tile 0)
+  const uint16_t* q_rope;  // [B, h, 64] bf16 or null
+  const int32_t* q_pos;
+  double theta;
+  int32_t* status;
+  long long wait_limit;
+};
+
+template <bool kAMajorMN>
+__global__ void __launch_bounds__(kGThreads)
+head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_x,
+                 const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int s = blockIdx.x, mt = blockIdx.y, nt = blockIdx.z;
+  const int b0 = nt * p.n_tile;
+  const int nk = p.K / kKChunk;
+  const int nstage = p.nstage;
+  const int kGStageBytes = p.stage_bytes;
+
+  const uint32_t bars = sbase + nstage * kGStageBytes;   // full[4], empty[4], done
+  auto full = [&](int i) { return bars + 8 * i; };
+  auto empty = [&](int i) { return bars + 8 * (kStagesG + i); };
+  const uint32_t done = bars + 8 * (2 * kStagesG);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + nstage * kGStageBytes + 128);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStagesG; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const long long lim = p.wait_limit;
+  bool ok = true;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    const uint32_t xbytes = (uint32_t)p.n_tile * kKChunk * 2;
+    for (int kc = 0; kc < nk; ++kc) {
+      const int st = kc % nstage;
+      if (kc >= nstage && !mbar_wait(empty(st), ((kc / nstage) - 1) & 1, lim)) {
+        ok = false;
+        break;
+      }
+      const uint32_t a_dst = sbase + st * kGStageBytes;
+      const uint32_t x_dst = a_dst + kABytes;
+      mbar_arrive_expect_tx(full(st), kABytes + xbytes);
+      if (kAMajorMN) {
+        // two boxes of 64 m (contiguous) x 64 k rows
+        tma_load_2d(a_dst, &tm_a, mt * 128, s * p.K + kc * kKChunk, full(st));
+        tma_load_2d(a_dst + kABytes / 2, &tm_a, mt * 128 + 64, s * p.K + kc * kKChunk, full(st));
+      } else {
+        // one box of 64 k (contiguous) x 128 m rows
+        tma_load_2d(a_dst, &tm_a, kc * kKChunk, s * 128 * gridDim.y + mt * 128, full(st));
+      }
+      tma_load_3d(x_dst, &tm_x, kc * kKChunk, s, b0, full(st));
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(128, p.n_tile, kAMajorMN, false);
+    for (int kc = 0; kc < nk && ok; ++kc) {
+      const int st = kc % nstage;
+      if (!mbar_wait(full(st), (kc / nstage) & 1, lim)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_st = sbase + st * kGStageBytes;
+      const uint32_t x_st = a_st + kABytes;
+#pragma unroll
+      for (int kk = 0; kk < kKChunk / 16; ++kk) {
+        const uint64_t ad = kAMajorMN ? smem_desc(a_st + kk * 2048, kABytes / 2, 1024, kSwizzle128B)
+                                      : smem_desc(a_st + kk * 32, 16, 1024, kSwizzle128B);
+        const uint64_t xd = smem_desc(x_st + kk * 32, 16, 1024, kSwizzle128B);
+        mma_ss(tmem, ad, xd, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(empty(st));
+    }
+    mma_commit(done);
+  }
+  __syncwarp();
+
+  // rotary query part (absorb, m tile 0): independent of the MMA
+  if (p.q_rope != nullptr && mt == 0) {
+    const int nb = min(p.n_tile, p.B - b0);
+    uint16_t* q_cat = static_cast<uint16_t*>(p.out);
+    for (int i = threadIdx.x; i < nb * 32; i += kGThreads) {
+      const int bb = b0 + i / 32, pr = i % 32;
+      const double inv = pow(p.theta, -2.0 * (double)pr / 64.0);
+      double sd, cd;
+      sincos((double)p.q_pos[bb] * inv, &sd, &cd);
+      const float cs = (float)cd, sn = (float)sd;
+      const int64_t ib = ((int64_t)bb * p.h + s) * 64;
+      const float x0 = bf16_to_f32(p.q_rope[ib + 2 * pr]);
+      const float x1 = bf16_to_f32(p.q_rope[ib + 2 * pr + 1]);
+      const int64_t ob = ((int64_t)bb * p.h + s) * p.out_ld + 512 + 2 * pr;
+      q_cat[ob] = f32_to_bf16_rn(x0 * cs - x1 * sn);
+      q_cat[ob + 1] = f32_to_bf16_rn(x0 * sn + x1 * cs);
+    }
+  }
+
+  // ------------------------------------------------------------ epilogue
+  // (every thread waits for the MMAs, even after a failure, so that TMEM is
+  // never released under a running MMA)
+  ok = __syncthreads_and(ok);
+  const bool waited = __syncthreads_and(mbar_wait(done, 0, lim));
+  if (!ok || !waited) {
+    if (threadIdx.x == 0) set_status(p.status, MLA_DEV_WAIT_TIMEOUT);
+  } else {
+    tc_fence_after();
+    const int m = warp * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    for (int c0 = 0; c0 < p.n_tile; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld16(tl + c0, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int b = b0 + c0 + e;
+        if (b < p.B) {
+          const int64_t o = ((int64_t)b * p.h + s) * p.out_ld + mt * 128 + m;
+          if (p.out_dtype == MLA_F32)
+            static_cast<float*>(p.out)[o] = __uint_as_float(v[e]);
+          else
+            static_cast<uint16_t*>(p.out)[o] = f32_to_bf16_rn(__uint_as_float(v[e]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+constexpr int kGSmemMax = kStagesG * (kABytes + kMaxN * kKChunk * 2) + 256 + 1024;
+
+// Pipeline shape for a contraction of K and a batch tile of n rows.
+void shape(GemmParams* p, int K, int n) {
+  p->K = K;
+  p->n_tile = n;
+  const int nk = K / kKChunk;
+  p->nstage = nk < kStagesG ? nk : kStagesG;
+  p->stage_bytes = (kABytes + n * kKChunk * 2 + 1023) / 1024 * 1024;
+  int c = 32;
+  while (c < n) c *= 2;
+  p->tmem_cols = c;
+}
+
+int smem_bytes(const GemmParams& p) { return p.nstage * p.stage_bytes + 256 + 1024; }
+
+bool encode(CUtensorMap* m, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int n_tile_for(int B) {
+  int n = B < kMaxN ? B : kMaxN;
+  return (n + 15) / 16 * 16;
+}
+
+template <bool kMN>
+cudaError_t set_smem_attr() {
+  static bool done = false;
+  if (!done) {
+    cudaError_t e = cudaFuncSetAttribute(head_gemm_kernel<kMN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemMax);
+    if (e != cudaSuccess) return e;
+    done = true;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int32_t* q_pos,
+                               const void* w_uk, void* q_cat, int B, int h, double theta,
+                               cudaStream_t s) {
+  // A: W_UK as [h * 128 (s, d) rows, 512 (c) cols]; boxes of 64 c x 64 d
+  CUtensorMap ta, tx;
+  cuuint64_t adims[2] = {512, (cuuint64_t)h * 128};
+  cuuint64_t astr[1] = {512 * 2};
+  cuuint32_t abox[2] = {64, 64};
+  // X: q_nope as (d = 128, s = h, b = B); boxes of 64 d x 1 x n_tile
+  const int nt = n_tile_for(B);
+  cuuint64_t xdims[3] = {128, (cuuint64_t)h, (cuuint64_t)B};
+  cuuint64_t xstr[2] = {128 * 2, (cuuint64_t)h * 128 * 2};
+  cuuint32_t xbox[3] = {64, 1, (cuuint32_t)nt};
+  if (!encode(&ta, 2, w_uk, adims, astr, abox) || !encode(&tx, 3, q_nope, xdims, xstr, xbox))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr<true>();
+  if (e != cudaSuccess) return e;
+  GemmParams p{};
+  shape(&p, 128, nt);
+  p.B = B;
+  p.h = h;
+  p.out = q_cat;
+  p.out_ld = 576;
+  p.out_dtype = MLA_BF16;
+  p.q_rope = static_cast<const uint16_t*>(q_rope);
+  p.q_pos = q_pos;
+  p.theta = theta;
+  p.status = nullptr;
+  p.wait_limit = 4000000000LL;
+  dim3 grid(h, 512 / 128, ceil_div(B, nt));
+  head_gemm_kernel<true><<<grid, kGThreads, smem_bytes(p), s>>>(ta, tx, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, int B, int h,
+                               int out_dtype, cudaStream_t s) {
+  // A: W_UV as [h * 128 (s, v) rows, 512 (c) cols]; boxes of 64 c x 128 v
+  CUtensorMap ta, tx;
+  cuuint64_t adims[2] = {512, (cuuint64_t)h * 128};
+  cuuint64_t astr[1] = {512 * 2};
+  cuuint32_t abox[2] = {64, 128};
+  const int nt = n_tile_for(B);
+  cuuint64_t xdims[3] = {512, (cuuint64_t)h, (cuuint64_t)B};
+  cuuint64_t xstr[2] = {512 * 2, (cuuint64_t)h * 512 * 2};
+  cuuint32_t xbox[3] = {64, 1, (cuuint32_t)nt};
+  if (!encode(&ta, 2, w_uv, adims, astr, abox) || !encode(&tx, 3, o_lat, xdims, xstr, xbox))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr<false>();
+  if (e != cudaSuccess) return e;
+  GemmParams p{};
+  shape(&p, 512, nt);
+  p.B = B;
+  p.h = h;
+  p.out = out;
+  p.out_ld = 128;
+  p.out_dtype = out_dtype;
+  p.q_rope = nullptr;
+  p.q_pos = nullptr;
+  p.theta = 0.0;
+  p.status = nullptr;
+  p.wait_limit = 4000000000LL;
+  dim3 grid(h, 1, ceil_div(B, nt));
+  head_gemm_kernel<false><<<grid, kGThreads, smem_bytes(p), s>>>(ta, tx, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

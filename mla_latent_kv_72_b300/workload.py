@@ -25,18 +25,10 @@ def storage_to_torch(a: np.ndarray, dtype: str, device) -> torch.Tensor:
     return t.to(device)
 
 
-def choose_num_splits(B: int, max_len: int, block_size: int, num_sms: int, heads_ctas: int = 1) -> int:
-    """Split count so that B * splits * heads_ctas fills the SMs about twice (capped
-    so that a split keeps at least 4 blocks)."""
-    nb = max(1, (max_len + block_size - 1) // block_size)
-    want = max(1, (2 * num_sms + B * heads_ctas - 1) // (B * heads_ctas))
-    return int(max(1, min(want, nb // 4 if nb >= 4 else 1, 1024)))
-
-
 class DeviceWorkload:
     """Everything one decode step reads and writes, resident on one GPU."""
 
-    def __init__(self, w: mi.Workload, device="cuda", num_splits: int | None = None,
+    def __init__(self, w: mi.Workload, device="cuda", num_parts: int | None = None,
                  rows_per_upload: int = 1 << 20, out_dtype=torch.float32):
         self.w = w
         self.device = torch.device(device)
@@ -73,14 +65,14 @@ class DeviceWorkload:
             self.kv = C.KVCache.packed(self.pool, d_c, d_r)
         self._fill(rows_per_upload)
 
-        if num_splits is None:
-            sms = torch.cuda.get_device_properties(dev).multi_processor_count
-            num_splits = choose_num_splits(w.B, self.max_len, bs, sms)
-        self.num_splits = num_splits
+        if num_parts is None:
+            num_parts = C.default_num_parts(dev)
+        self.num_parts = int(num_parts)
         B, h = w.B, w.h
+        nslot = C.mla_decode_num_partials(B, self.num_parts)
         self.q_cat = torch.empty((B, h, d_c + d_r), dtype=tdt, device=dev)
-        self.o_part = torch.empty((B, num_splits, h, d_c), dtype=torch.float32, device=dev)
-        self.lse_part = torch.empty((B, num_splits, h), dtype=torch.float32, device=dev)
+        self.o_part = torch.empty((nslot, h, d_c), dtype=torch.float32, device=dev)
+        self.lse_part = torch.empty((nslot, h), dtype=torch.float32, device=dev)
         self.o_lat = torch.empty((B, h, d_c), dtype=tdt, device=dev)
         self.lse = torch.empty((B, h), dtype=torch.float32, device=dev)
         self.out = torch.empty((B, h, w.d_v), dtype=out_dtype, device=dev)
@@ -117,11 +109,14 @@ class DeviceWorkload:
                        rope_theta=self.w.theta, stream=stream)
 
     def attend(self, flags=C.MLA_DECODE_AUTO, stream=None):
-        C.mla_decode_fwd(self.q_cat, self.kv, self.block_table, self.seq_lens, self.o_part,
-                         self.lse_part, dev_status=self.status, flags=flags, stream=stream)
+        C.mla_decode_fwd(self.q_cat, self.kv, self.block_table, self.seq_lens, self.num_parts,
+                         self.o_part, self.lse_part, dev_status=self.status, flags=flags,
+                         stream=stream)
 
     def combine(self, stream=None):
-        C.mla_combine(self.o_part, self.lse_part, self.o_lat, self.lse, stream=stream)
+        C.mla_combine(self.o_part, self.lse_part, self.seq_lens, self.w.block_size,
+                      self.block_table.shape[1], self.num_parts, self.o_lat, self.lse,
+                      stream=stream)
 
     def project(self, stream=None):
         C.mla_out_proj(self.o_lat, self.w_uv, self.out, stream=stream)

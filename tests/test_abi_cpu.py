@@ -99,7 +99,7 @@ def test_decode_fwd_host_checks(lib):
     assert call(ns=0) == -1
     assert call(maxb=0) == -1
     assert call(flags=7) == -1
-    assert call(ns=5000) == -4
+    assert call(ns=1025) == -4
     assert call(kv=_kv(nblk=0)) == -1
     assert call(kv=_kv(d_c=500)) == -4
     assert call(kv=_kv(latent=MIS)) == -2
@@ -113,13 +113,29 @@ def test_decode_fwd_host_checks(lib):
     assert call(q=MIS) == -2
 
 
+def test_decode_num_partials(lib):
+    assert lib.mla_decode_num_partials(64, 74) == 137
+    assert lib.mla_decode_num_partials(1, 1) == 1
+    assert lib.mla_decode_num_partials(0, 4) == -1
+    assert lib.mla_decode_num_partials(4, 0) == -1
+    assert lib.mla_decode_num_partials(4, 1025) == -1
+
+
 def test_combine_and_out_proj_host_checks(lib):
     c = lib.mla_combine
-    assert c(None, A, 2, 4, 512, 2, A, M.MLA_F32, None, None) == -1
-    assert c(A, A, 2, 4, 512, 0, A, M.MLA_F32, None, None) == -1
-    assert c(A, A, 2, 4, 510, 2, A, M.MLA_F32, None, None) == -4
-    assert c(A, A, 2, 4, 512, 2, A, M.MLA_FP8E4M3, None, None) == -3
-    assert c(A, A, 2, 4, 512, 2, MIS, M.MLA_F32, None, None) == -2
+
+    def call(op=A, seq=A, bs=64, maxb=4, B=2, h=4, d_c=512, parts=2, o=A, odt=M.MLA_F32):
+        return c(op, A, seq, bs, maxb, B, h, d_c, parts, o, odt, None, None)
+
+    assert call(op=None) == -1
+    assert call(seq=None) == -1
+    assert call(parts=0) == -1
+    assert call(bs=0) == -1
+    assert call(maxb=0) == -1
+    assert call(d_c=510) == -4
+    assert call(parts=2000) == -4
+    assert call(odt=M.MLA_FP8E4M3) == -3
+    assert call(o=MIS) == -2
     o = lib.mla_out_proj
     assert o(None, A, A, 2, 4, 512, 128, 1, 0, None) == -1
     assert o(A, A, A, 2, 4, 512, 0, 1, 0, None) == -1

@@ -88,7 +88,7 @@ def test_small_workloads_match_oracle(name, flags):
 def test_edge_lengths(L):
     w = mi.scaled(mi.workload(3), B=2, h=16, L=L)
     for ns in (1, 3):
-        dw = make(w, num_splits=ns)
+        dw = make(w, num_parts=ns)
         dw.step()
         torch.cuda.synchronize()
         compare(w, dw, range(w.B), None, TOL["bf16"])
@@ -105,29 +105,63 @@ def test_fp32_tolerance_is_tight():
 
 
 # ----------------------------------------------------------------------------
-# split-KV and paging invariants
+# part partition, split-KV and paging invariants
 # ----------------------------------------------------------------------------
 
-def test_split_count_invariance():
+def expected_slots(lens, block_size, num_parts):
+    """Partial slots p + b written under the part partition (its definition in
+    include/mla72.h, restated here on the host)."""
+    nb = [(int(L) + block_size - 1) // block_size for L in lens]
+    T = sum(nb)
+    P = min(num_parts, T)
+    bounds = [p * T // P for p in range(P + 1)]
+    slots = set()
+    start = 0
+    for b, n in enumerate(nb):
+        for g in range(start, start + n):
+            p = max(q for q in range(P) if bounds[q] <= g)
+            slots.add(p + b)
+        start += n
+    return slots
+
+
+@pytest.mark.parametrize("num_parts", [1, 2, 7, 64, 148])
+def test_part_count_invariance(num_parts):
     w = mi.scaled(mi.workload(3), B=2, h=128, L=3000)
-    ref = None
-    for ns in (1, 2, 7, 64):
-        dw = make(w, num_splits=ns)
-        dw.step()
-        torch.cuda.synchronize()
-        o = dw.o_lat.float().cpu().numpy()
-        if ref is None:
-            ref = o
-        else:
-            assert np.abs(o - ref).max() / np.abs(ref).max() < 1e-2
+    dw1 = make(w, num_parts=1)
+    dw1.step()
+    dw = make(w, num_parts=num_parts)
+    dw.step()
+    torch.cuda.synchronize()
+    ref = dw1.o_lat.float().cpu().numpy()
+    o = dw.o_lat.float().cpu().numpy()
+    assert np.abs(o - ref).max() / np.abs(ref).max() < 1e-2
     compare(w, dw, range(w.B), [0, 77, 127], TOL["bf16"])
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["auto", "simt"])
+def test_partial_slots_follow_the_partition(flags):
+    # variable lengths, more parts than some sequences have blocks, and more
+    # parts than the whole stream (16 sequences, 200 parts)
+    w = mi.scaled(mi.workload(4), B=16, h=16, L_range=(1, 400))
+    for num_parts in (5, 37, 200):
+        dw = make(w, num_parts=num_parts)
+        dw.o_part.fill_(float("nan"))
+        dw.lse_part.fill_(float("nan"))
+        dw.step(flags=flags)
+        torch.cuda.synchronize()
+        assert dw.check_status() == 0
+        want = expected_slots(dw.lens_np, w.block_size, num_parts)
+        written = ~torch.isnan(dw.lse_part[:, 0]).cpu().numpy()
+        assert set(np.nonzero(written)[0].tolist()) == want
+        compare(w, dw, range(w.B), None, TOL["bf16"])
 
 
 def test_paged_permutation_is_bit_exact():
     base = mi.scaled(mi.workload(4), B=4, L_range=(100, 900))
     contig = mi.scaled(base, layout="contiguous")
-    a = make(base, num_splits=3)
-    b = make(contig, num_splits=3)
+    a = make(base, num_parts=3)
+    b = make(contig, num_parts=3)
     assert not np.array_equal(a.table_np, b.table_np)
     for dw in (a, b):
         dw.step()
@@ -136,19 +170,9 @@ def test_paged_permutation_is_bit_exact():
     assert torch.equal(a.out.view(torch.int32), b.out.view(torch.int32))
 
 
-def test_empty_splits_are_harmless():
-    w = mi.scaled(mi.workload(3), B=2, h=16, L=100)      # 2 blocks, 16 splits
-    dw = make(w, num_splits=16)
-    dw.step()
-    torch.cuda.synchronize()
-    lse_part = dw.lse_part.cpu().numpy()
-    assert np.isneginf(lse_part).any()
-    compare(w, dw, range(w.B), None, TOL["bf16"])
-
-
 def test_bad_block_is_reported_not_dereferenced():
     w = mi.scaled(mi.workload(3), B=2, h=16, L=200)
-    dw = make(w, num_splits=1)
+    dw = make(w, num_parts=1)
     dw.block_table[1, 1] = dw.num_blocks + 1000
     dw.step()
     torch.cuda.synchronize()
