@@ -57,12 +57,10 @@ constexpr int kTok = 64;                    // tokens per tile (= cache block)
 constexpr int kStages = 3;
 constexpr int kBoxBytes = 64 * 128;         // 64 rows x 64 bf16, 128-byte swizzle
 constexpr int kStageBytes = 5 * kBoxBytes;  // CTA 0: 4 latent boxes + the RoPE box
-constexpr int kPBytes = 128 * 128;          // P: 128 rows x 64 bf16
 constexpr int kRecvBytes = 128 * 64 * 4;    // partial S of the peer, float32
 
 constexpr int kOffStages = 0;
-constexpr int kOffP = kOffStages + kStages * kStageBytes;
-constexpr int kOffRecv = kOffP + 2 * kPBytes;
+constexpr int kOffRecv = kOffStages + kStages * kStageBytes;
 constexpr int kOffMpub = kOffRecv + 2 * kRecvBytes;     // [2][128] float
 constexpr int kOffLstate = kOffMpub + 2 * 128 * 4;      // [2 seg][2 group][128] float2
 constexpr int kOffBar = kOffLstate + 2 * 2 * 128 * 8;
@@ -75,6 +73,7 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS = 256;
 constexpr uint32_t kColQ = 320;
+constexpr uint32_t kColP = 480;   // P (bf16 pairs), A operand of the P.C MMA
 constexpr uint32_t kTmemCols = 512;
 
 constexpr int kThreads = 320;
@@ -116,6 +115,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+
+// Optional per-tile event timestamps for pipeline analysis (compiled only with
+// -DMLA_TRACE; the product build has none of it).
+#ifdef MLA_TRACE
+constexpr int kTraceTiles = 128;
+constexpr int kTraceEv = 12;
+__device__ unsigned long long* g_trace = nullptr;
+#define MLA_TR(k, ev)                                                                   \
+  do {                                                                                  \
+    if (g_trace != nullptr && part < 2 && (k) < kTraceTiles)                            \
+      g_trace[((part * 2 + rank) * kTraceTiles + (k)) * kTraceEv + (ev)] = clock64();   \
+  } while (0)
+#else
+#define MLA_TR(k, ev) \
+  do {                \
+  } while (0)
+#endif
 
 // Walks the part's tiles (sequence b, logical block blk) in stream order.
 struct TileIter {
@@ -259,6 +275,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           set_status(p.status, MLA_DEV_BAD_BLOCK);
           pb = 0;  // load a valid block instead; the result is flagged as wrong
         }
+        MLA_TR(k, 0);
         const uint32_t dst = sbase + kOffStages + st * kStageBytes;
         const uint32_t fb = bar(BAR_KV_FULL + st);
         mbar_arrive_expect_tx(fb, tx);
@@ -280,76 +297,101 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     }
   } else if (b_first >= 0 && ntiles > 0 && warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Event-driven: whichever of the next score MMA S(ks) and the next P.C MMA
+    // O(ko) has its inputs ready is issued first, so a late P never holds back
+    // the next score tile (lane 0 probes, the warp follows its decision).
     const uint32_t idS = idesc_bf16_f32(128, 64, false, false);
     const uint32_t idO = idesc_bf16_f32(128, 256, false, true);
     const int nK = rank == 0 ? 20 : 16;     // 16-wide K steps of the partial score
     const int nbox = rank == 0 ? 5 : 4;
-    TileIter it;
-    it.init(p.seq_lens, p.max_blocks, b_first, blk_first);
-
-    // O += P(j) C(j); the first tile of a segment overwrites O
-    auto issue_o = [&](int j, bool first_j, int seg_j) -> bool {
-      if (first_j && seg_j > 0 && !warp_wait(bar(BAR_O_FREE), (seg_j - 1) & 1)) return false;
-      if (!warp_wait(bar(BAR_P_FULL + (j & 1)), (j >> 1) & 1)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t stage = sbase + kOffStages + (j % kStages) * kStageBytes;
-        const uint32_t pbuf = sbase + kOffP + (j & 1) * kPBytes;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint64_t ad = smem_desc(pbuf + c * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(stage + c * 2048, kBoxBytes, 1024, kSwizzle128B);
-          mma_ss(tmem + kColO, ad, bd, idO, (first_j && c == 0) ? 0u : 1u);
-        }
-        mma_commit(bar(BAR_O_DONE + (j & 1)));
-        mma_commit(bar(BAR_KV_EMPTY + (j % kStages)));
-      }
-      __syncwarp();
-      return true;
-    };
-
+    TileIter its, ito;
+    its.init(p.seq_lens, p.max_blocks, b_first, blk_first);
+    ito.init(p.seq_lens, p.max_blocks, b_first, blk_first);
+    int ks = 0, ko = 0, seg_s = 0, seg_o = 0;
+    long long idle_since = clock64();
     bool ok = true;
-    int seg = 0, prev_seg = 0;
-    bool prev_first = false;
-    for (int k = 0; k < ntiles; ++k) {
-      const bool first = (k == 0) || (it.blk == 0);
-      const bool last = (k == ntiles - 1) || (it.blk == it.nb - 1);
-      const int st = k % kStages;
-      if (first && !warp_wait(bar(BAR_Q_READY), seg & 1)) { ok = false; break; }
-      if (!warp_wait(bar(BAR_KV_FULL + st), (k / kStages) & 1)) { ok = false; break; }
-      const int n_valid = it.valid();
-      if (n_valid < kTok) {
-        // slots past the sequence end: zero them so that P = 0 meets finite values
-        uint8_t* sp = smem + kOffStages + st * kStageBytes;
-        const int nrow = kTok - n_valid;
-        for (int e = lane; e < nbox * nrow * 8; e += 32) {
-          const int box = e / (nrow * 8), rr = (e / 8) % nrow, ch = e % 8;
-          *reinterpret_cast<uint4*>(sp + box * kBoxBytes + (n_valid + rr) * 128 + ch * 16) =
-              make_uint4(0, 0, 0, 0);
+    while (ko < ntiles) {
+      bool did = false;
+      if (ks < ntiles) {
+        const int st = ks % kStages;
+        const bool first = (ks == 0) || (its.blk == 0);
+        const bool last = (ks == ntiles - 1) || (its.blk == its.nb - 1);
+        bool ready = true;
+        if (lane == 0)
+          ready = (!first || mbar_test_wait(bar(BAR_Q_READY), seg_s & 1)) &&
+                  mbar_test_wait(bar(BAR_KV_FULL + st), (ks / kStages) & 1) &&
+                  (ks == 0 || mbar_test_wait(bar(BAR_S_EMPTY), (ks - 1) & 1));
+        if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) {
+          const int n_valid = its.valid();
+          if (n_valid < kTok) {
+            // slots past the sequence end: zero them so that P = 0 meets finite values
+            uint8_t* sp = smem + kOffStages + st * kStageBytes;
+            const int nrow = kTok - n_valid;
+            for (int e = lane; e < nbox * nrow * 8; e += 32) {
+              const int box = e / (nrow * 8), rr = (e / 8) % nrow, ch = e % 8;
+              *reinterpret_cast<uint4*>(sp + box * kBoxBytes + (n_valid + rr) * 128 + ch * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          tc_fence_after();
+          if (lane == 0) {
+            MLA_TR(ks, 1);
+            const uint32_t stage = sbase + kOffStages + st * kStageBytes;
+            for (int kk = 0; kk < nK; ++kk) {
+              const uint64_t bd = smem_desc(stage + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16,
+                                            1024, kSwizzle128B);
+              mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bd, idS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar(BAR_S_FULL + (ks & 1)));
+            if (last) mma_commit(bar(BAR_Q_FREE));
+          }
+          __syncwarp();
+          if (last) ++seg_s;
+          if (ks + 1 < ntiles) its.next();
+          ++ks;
+          did = true;
         }
-        fence_proxy_async_smem();
       }
-      __syncwarp();
-      if (k > 0 && !warp_wait(bar(BAR_S_EMPTY), (k - 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t stage = sbase + kOffStages + st * kStageBytes;
-        for (int kk = 0; kk < nK; ++kk) {
-          const uint64_t bd = smem_desc(stage + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024,
-                                        kSwizzle128B);
-          mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bd, idS, kk > 0 ? 1u : 0u);
+      if (ko < ks) {
+        const bool first = (ko == 0) || (ito.blk == 0);
+        const bool last = (ko == ntiles - 1) || (ito.blk == ito.nb - 1);
+        bool ready = true;
+        if (lane == 0)
+          ready = (!(first && seg_o > 0) || mbar_test_wait(bar(BAR_O_FREE), (seg_o - 1) & 1)) &&
+                  mbar_test_wait(bar(BAR_P_FULL + (ko & 1)), (ko >> 1) & 1);
+        if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) {
+          tc_fence_after();
+          if (lane == 0) {
+            MLA_TR(ko, 2);
+            const uint32_t stage = sbase + kOffStages + (ko % kStages) * kStageBytes;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint64_t bd = smem_desc(stage + c * 2048, kBoxBytes, 1024, kSwizzle128B);
+              mma_ts(tmem + kColO, tmem + kColP + 8 * c, bd, idO, (first && c == 0) ? 0u : 1u);
+            }
+            mma_commit(bar(BAR_O_DONE + (ko & 1)));
+            mma_commit(bar(BAR_KV_EMPTY + (ko % kStages)));
+          }
+          __syncwarp();
+          if (last) ++seg_o;
+          if (ko + 1 < ntiles) ito.next();
+          ++ko;
+          did = true;
         }
-        mma_commit(bar(BAR_S_FULL + (k & 1)));
-        if (last) mma_commit(bar(BAR_Q_FREE));
       }
-      __syncwarp();
-      if (k > 0 && !issue_o(k - 1, prev_first, prev_seg)) { ok = false; break; }
-      prev_first = first;
-      prev_seg = seg;
-      if (last) ++seg;
-      if (k + 1 < ntiles) it.next();
+      if (did) {
+        idle_since = clock64();
+      } else {
+        if (*abort_flag) { ok = false; break; }
+        if (clock64() - idle_since > lim) {
+          timed_out = true;
+          ok = false;
+          break;
+        }
+      }
     }
-    if (ok) ok = issue_o(ntiles - 1, prev_first, prev_seg);
     if (!ok) fail();
     // drain: every MMA issued by this thread has completed
     if (lane == 0) {
@@ -367,12 +409,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
     const bool live = row < p.h;
     const bool group_lead = (warp == 2 + 4 * g) && lane == 0;
-    const int sw16 = row & 15, sw8 = row & 7;
     float* mpub = reinterpret_cast<float*>(smem + kOffMpub);
     float2* lstate = reinterpret_cast<float2*>(smem + kOffLstate);
-    const uint32_t my_recv_u32 = sbase + kOffRecv + g * kRecvBytes + row * 256;
-    const uint8_t* my_recv = smem + kOffRecv + g * kRecvBytes + row * 256;
-    const uint32_t peer_recv = mapa(my_recv_u32, peer);
+    // exchange buffers: chunk c (16 B) of row sub * 32 + lane at
+    // sub * 8192 + c * 512 + lane * 16, so that a warp's stores and loads are
+    // contiguous 512-byte runs
+    const uint32_t xoff = (uint32_t)(sub * 8192 + lane * 16);
+    const uint8_t* my_recv = smem + kOffRecv + g * kRecvBytes + xoff;
+    const uint32_t peer_recv = mapa(sbase + kOffRecv + g * kRecvBytes + xoff, peer);
     const uint32_t peer_recv_full = mapa(bar(BAR_RECV_FULL + g), peer);
     const uint32_t peer_free = mapa(bar(BAR_PEER_FREE + g), peer);
 
@@ -418,6 +462,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         const int n_valid = it.valid();
         // ---- partial scores of this CTA
         if (!warp_wait(bar(BAR_S_FULL + g), u & 1)) { ok = false; break; }
+        if (group_lead) MLA_TR(k, 3);
         tc_fence_after();
         uint32_t r[64];
         tmem_ld16(tl + kColS + 0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
@@ -433,18 +478,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (u >= 1 && !warp_wait_cluster(bar(BAR_PEER_FREE + g), (u - 1) & 1)) { ok = false; break; }
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          st_cluster_v4(peer_recv + ((c ^ sw16) << 4), __uint_as_float(r[4 * c]),
+          st_cluster_v4(peer_recv + c * 512, __uint_as_float(r[4 * c]),
                         __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
                         __uint_as_float(r[4 * c + 3]));
         // one release arrive per warp publishes the warp's 32 rows to the peer
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(peer_recv_full);
+        if (group_lead) MLA_TR(k, 4);
         if (!warp_wait_cluster(bar(BAR_RECV_FULL + g), u & 1)) { ok = false; break; }
+        if (group_lead) MLA_TR(k, 5);
         // full score (log2 domain) in place: r <- (own partial + peer's) * scale
         float mt = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float4 v = *reinterpret_cast<const float4*>(my_recv + ((c ^ sw16) << 4));
+          const float4 v = *reinterpret_cast<const float4*>(my_recv + c * 512);
           const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -465,6 +512,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           if (!warp_wait(bar(BAR_MREADY + (kp & 1)), (kp >> 1) & 1)) { ok = false; break; }
           m_prev = mpub[(kp & 1) * 128 + row];
         }
+        if (group_lead) MLA_TR(k, 6);
         float m_k = m_prev;
         bool resc = false;
         if (m_prev == -INFINITY) {
@@ -481,16 +529,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           m_g = m_k;
         }
 
-        // ---- P buffer (k & 1) was last read by the P.C MMA of tile k-2; waiting
-        // for it first also means O(k-3) is done, so the wait on the other
-        // group's O_DONE below cannot alias an older phase
+        // ---- P (bf16 pairs) in registers first, overlapping the P.C MMA of tile k-1
+        uint32_t pk[32];
+        float psum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = exp2f(__uint_as_float(r[2 * e]) - m_k);
+          const float p1 = exp2f(__uint_as_float(r[2 * e + 1]) - m_k);
+          psum += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        l_g += psum;
+
+        // ---- the single TMEM P buffer was read by the P.C MMA of tile k-1; wait
+        // for it (first for tile k-2 on this group's own barrier, so that the
+        // wait on the other group's barrier cannot alias an older phase)
         if (k >= 2 && !warp_wait(bar(BAR_O_DONE + (k & 1)), ((k - 2) >> 1) & 1)) { ok = false; break; }
+        if (k >= 1 && !warp_wait(bar(BAR_O_DONE + ((k - 1) & 1)), ((k - 1) >> 1) & 1)) { ok = false; break; }
+        if (group_lead) MLA_TR(k, 7);
+        tc_fence_after();
 
         // ---- rescale O between P(k-1) C and P(k) C (rare)
         if (__any_sync(0xffffffffu, resc)) {
-          const int kp = k - 1;
-          if (!warp_wait(bar(BAR_O_DONE + (kp & 1)), (kp >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
           const float alpha = resc ? exp2f(m_prev - m_k) : 1.0f;
           for (int c = 0; c < 16; ++c) {
             uint32_t v[16];
@@ -500,29 +560,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
             tmem_st16(tl + kColO + 16 * c, v);
           }
-          tmem_wait_st();
         }
-
-        // ---- P (bf16)
-        uint8_t* prow = smem + kOffP + (k & 1) * kPBytes + row * 128;
-        float psum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = exp2f(__uint_as_float(r[8 * c + 2 * e]) - m_k);
-            const float p1 = exp2f(__uint_as_float(r[8 * c + 2 * e + 1]) - m_k);
-            psum += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
-          }
-          *reinterpret_cast<uint4*>(prow + ((c ^ sw8) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        l_g += psum;
-        fence_proxy_async_smem();
+        tmem_st16(tl + kColP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(tl + kColP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_P_FULL + (k & 1)));
+        if (group_lead) MLA_TR(k, 8);
       }
 
       if (last) {
@@ -623,6 +668,12 @@ int device_major() {
 }
 
 }  // namespace
+
+#ifdef MLA_TRACE
+extern "C" int mla_debug_set_trace(void* p) {
+  return cudaMemcpyToSymbol(g_trace, &p, sizeof(p)) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
