@@ -213,6 +213,31 @@ int mla_combine(const float* o_part, const float* lse_part, const int32_t* seq_l
                 void* o_lat, int o_dtype, float* lse, void* stream);
 
 /*
+ * mla_decode_attend_noalloc: mla_decode_fwd followed by mla_combine, for
+ * callers that cannot allocate device memory (code running under another
+ * framework's allocator or memory pool, or a runtime that forbids cudaMalloc
+ * on its hot path).  The pages have no counterpart: this is a packaging of
+ * the same two calls, not part of the method.
+ *
+ * The split partials live in a file-scope device array of the library
+ * instead of caller buffers; the caller passes only inputs and outputs
+ * (arguments as for mla_decode_fwd, then o_lat [B, h, d_c] in o_dtype and
+ * lse [B, h] float32 or NULL, as for mla_combine).  Limits: with
+ * S = B + num_parts - 1 partial slots, S * h * d_c <= 16 Mi and S * h <= 1 Mi
+ * (the array holds 68 MiB on every device that loads the library, until the
+ * process exits); larger calls return MLA_ERR_SHAPE and launch nothing.
+ * The first call on a device looks up the array's device address with that
+ * device current; make it before any stream capture.  All calls share the
+ * array: calls that overlap on the GPU race on it.  Nothing in it needs to
+ * start at zero (each call writes every slot it reads).  Allocates nothing.
+ */
+int mla_decode_attend_noalloc(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
+                              const int32_t* block_table, int max_blocks_per_seq,
+                              const int32_t* seq_lens, int B, int h, int num_parts,
+                              float softmax_scale, void* o_lat, int o_dtype, float* lse,
+                              int32_t* dev_status, void* stream);
+
+/*
  * mla_out_proj: W_UV applied after attention (kexue.fm section "Part 1": W_v
  * is absorbed into the projection that follows o_t; eq. mla-mqa first line
  * o_t = [o^(1) W_v^(1), ..., o^(h) W_v^(h)]; iotdigitaltwinplm.com absorbed

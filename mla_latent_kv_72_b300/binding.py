@@ -23,8 +23,8 @@ _LIB = None
 
 EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_version", "mla_cache_bytes_per_token", "mla_absorb_q",
-    "mla_decode_num_partials", "mla_decode_fwd", "mla_combine", "mla_out_proj",
-    "mla_cache_fill", "mla_paged_gather",
+    "mla_decode_num_partials", "mla_decode_fwd", "mla_combine", "mla_decode_attend_noalloc",
+    "mla_out_proj", "mla_cache_fill", "mla_paged_gather",
 )
 
 
@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
         "mla_decode_num_partials": (i32, [i32, i32]),
         "mla_decode_fwd": (i32, [vp, i32, kvp, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp, u32, vp]),
         "mla_combine": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp]),
+        "mla_decode_attend_noalloc": (i32, [vp, i32, kvp, vp, i32, vp, i32, i32, i32, f32, vp, i32,
+                                            vp, vp, vp]),
         "mla_out_proj": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
         "mla_cache_fill": (i32, [vp, vp, i32, vp, i32, i32, vp, i32, kvp, f64, vp, vp]),
         "mla_paged_gather": (i32, [kvp, vp, i32, vp, i32, i32, vp, vp, vp, vp]),
@@ -192,6 +194,18 @@ def mla_combine(o_part, lse_part, seq_lens, block_size, max_blocks_per_seq, num_
         _ptr(o_part), _ptr(lse_part), _ptr(seq_lens), int(block_size), int(max_blocks_per_seq),
         B, h, d_c, int(num_parts), _ptr(o_lat), dtype_code(o_lat.dtype), _ptr(lse),
         _stream(stream)))
+    return o_lat
+
+
+def mla_decode_attend_noalloc(q_cat, kv: KVCache, block_table, seq_lens, num_parts, o_lat,
+                              lse=None, *, softmax_scale=0.0, dev_status=None, stream=None):
+    """mla_decode_fwd + mla_combine with the partials in the library's own
+    device array, for callers that cannot allocate (see mla72.h)."""
+    B, h, _ = q_cat.shape
+    _check("mla_decode_attend_noalloc", lib().mla_decode_attend_noalloc(
+        _ptr(q_cat), dtype_code(q_cat.dtype), ctypes.byref(kv), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, h, int(num_parts), float(softmax_scale),
+        _ptr(o_lat), dtype_code(o_lat.dtype), _ptr(lse), _ptr(dev_status), _stream(stream)))
     return o_lat
 
 
