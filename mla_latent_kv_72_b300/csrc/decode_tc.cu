@@ -54,17 +54,20 @@ namespace {
 using namespace tc;
 
 constexpr int kTok = 64;                    // tokens per tile (= cache block)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kBoxBytes = 64 * 128;         // 64 rows x 64 bf16, 128-byte swizzle
-constexpr int kStageBytes = 5 * kBoxBytes;  // CTA 0: 4 latent boxes + the RoPE box
+constexpr int kRopeBoxBytes = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
+constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // 4 latent boxes + half the RoPE dims
+constexpr int kQRopeBytes = 128 * 64;       // query RoPE slice: 128 heads x 32 bf16
 constexpr int kRecvBytes = 128 * 64 * 4;    // partial S of the peer, float32
 
 constexpr int kOffStages = 0;
 constexpr int kOffRecv = kOffStages + kStages * kStageBytes;
-constexpr int kOffMpub = kOffRecv + 2 * kRecvBytes;     // [2][128] float
+constexpr int kOffQRope = kOffRecv + 2 * kRecvBytes;    // 1024-aligned
+constexpr int kOffMpub = kOffQRope + kQRopeBytes;       // [2][128] float
 constexpr int kOffLstate = kOffMpub + 2 * 128 * 4;      // [2 seg][2 group][128] float2
 constexpr int kOffBar = kOffLstate + 2 * 2 * 128 * 8;
-constexpr int kNumBars = 24;
+constexpr int kNumBars = 32;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64;
 constexpr int kSmemAlloc = kSmemBytes + 1024;  // alignment slack
@@ -72,32 +75,35 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS = 256;
-constexpr uint32_t kColQ = 320;
-constexpr uint32_t kColP = 480;   // P (bf16 pairs), A operand of the P.C MMA
+constexpr uint32_t kColQ = 320;   // latent query slice (bf16 pairs), 128 columns
+constexpr uint32_t kColP = 448;   // [2] P (bf16 pairs, 32 columns each), A of the P.C MMA
 constexpr uint32_t kTmemCols = 512;
 
 constexpr int kThreads = 320;
 constexpr float kTau = 8.0f;  // lazy rescale threshold (log2 units): P stays <= 2^8
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// barrier indices
+// barrier indices (derived from kStages so that the arrays never overlap)
 enum {
-  BAR_KV_FULL = 0,    // [kStages] TMA -> MMA
-  BAR_KV_EMPTY = 3,   // [kStages] MMA (commit after P.C) -> TMA
-  BAR_S_FULL = 6,     // [2] MMA -> softmax group (k & 1); one barrier per group so that
-                      //     a group's parity waits never alias the other group's phases
-  BAR_S_EMPTY = 8,    // softmax (4 warps) -> MMA
-  BAR_P_FULL = 9,     // [2] softmax (4 warps) -> MMA
-  BAR_O_DONE = 11,    // [2] MMA -> softmax (P buffer free, O final)
-  BAR_RECV_FULL = 13, // [2] peer's 4 warps have written their partial scores here
-  BAR_PEER_FREE = 15, // [2] peer's 4 warps have read what we sent
-  BAR_MREADY = 17,    // [2] running maximum of a tile published (4 warps)
-  BAR_Q_FREE = 19,    // MMA: last score MMA of a segment done
-  BAR_Q_READY = 20,   // softmax (8 warps): query slice of a segment in TMEM
-  BAR_O_FREE = 21,    // softmax (8 warps): O of a segment read out
-  BAR_SEG = 22,       // softmax (8 warps): end-of-segment rendezvous
-  BAR_DRAIN = 23,
+  BAR_KV_FULL = 0,                      // [kStages] TMA -> MMA
+  BAR_KV_EMPTY = BAR_KV_FULL + kStages, // [kStages] MMA (commit after P.C) -> TMA
+  BAR_S_FULL = BAR_KV_EMPTY + kStages,  // [2] MMA -> softmax group (k & 1); one barrier per
+                                        //     group so that a group's parity waits never
+                                        //     alias the other group's phases
+  BAR_S_EMPTY = BAR_S_FULL + 2,         // softmax (4 warps) -> MMA
+  BAR_P_FULL = BAR_S_EMPTY + 1,         // [2] softmax (4 warps) -> MMA
+  BAR_O_DONE = BAR_P_FULL + 2,          // [2] MMA -> softmax (P buffer free, O final)
+  BAR_RECV_FULL = BAR_O_DONE + 2,       // [2] peer's 4 warps have written their partial scores
+  BAR_PEER_FREE = BAR_RECV_FULL + 2,    // [2] peer's 4 warps have read what we sent
+  BAR_MREADY = BAR_PEER_FREE + 2,       // [2] running maximum of a tile published (4 warps)
+  BAR_Q_FREE = BAR_MREADY + 2,          // MMA: last score MMA of a segment done
+  BAR_Q_READY = BAR_Q_FREE + 1,         // softmax (8 warps) + TMA of the RoPE query slice
+  BAR_O_FREE = BAR_Q_READY + 1,         // softmax (8 warps): O of a segment read out
+  BAR_SEG = BAR_O_FREE + 1,             // softmax (8 warps): end-of-segment rendezvous
+  BAR_DRAIN = BAR_SEG + 1,
+  BAR_COUNT = BAR_DRAIN + 1,
 };
+static_assert(BAR_COUNT <= kNumBars, "barrier array");
 
 struct TcParams {
   const uint16_t* q_cat;        // [B, h, 576] bf16
@@ -127,9 +133,17 @@ __device__ unsigned long long* g_trace = nullptr;
     if (g_trace != nullptr && part < 2 && (k) < kTraceTiles)                            \
       g_trace[((part * 2 + rank) * kTraceTiles + (k)) * kTraceEv + (ev)] = clock64();   \
   } while (0)
+#define MLA_SITE(site)                                                                  \
+  do {                                                                                  \
+    if (g_trace != nullptr && part < 2)                                                 \
+      g_trace[((part * 2 + rank) * kTraceTiles + kTraceTiles - 1) * kTraceEv + 11] = (site); \
+  } while (0)
 #else
 #define MLA_TR(k, ev) \
   do {                \
+  } while (0)
+#define MLA_SITE(site) \
+  do {                 \
   } while (0)
 #endif
 
@@ -166,7 +180,8 @@ struct TileIter {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
-                 const __grid_constant__ CUtensorMap tm_rope, const TcParams p) {
+                 const __grid_constant__ CUtensorMap tm_rope,
+                 const __grid_constant__ CUtensorMap tm_q, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -196,7 +211,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       mbar_init(bar(BAR_MREADY + i), 4);
     }
     mbar_init(bar(BAR_Q_FREE), 1);
-    mbar_init(bar(BAR_Q_READY), 8);
+    mbar_init(bar(BAR_Q_READY), 9);
     mbar_init(bar(BAR_O_FREE), 8);
     mbar_init(bar(BAR_SEG), 8);
     mbar_init(bar(BAR_DRAIN), 1);
@@ -221,6 +236,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       info[2] = (int)(g1 - g0);
       prefetch_tmap(&tm_lat);
       prefetch_tmap(&tm_rope);
+      prefetch_tmap(&tm_q);
       if (part == 0 && rank == 0)
         for (int b = 0; b < p.B; ++b)
           if (p.seq_lens[b] > p.max_blocks * kTok) set_status(p.status, MLA_DEV_BAD_LENGTH);
@@ -245,12 +261,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
   // lane 0 waits, the warp learns the result
   auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
     bool ok = true;
-    if (lane == 0) ok = mbar_wait_or_abort(b, parity, lim, abort_flag, &timed_out);
+    if (lane == 0) {
+      ok = mbar_wait_or_abort(b, parity, lim, abort_flag, &timed_out);
+      if (!ok && timed_out) MLA_SITE(1000 + warp * 100 + (int)((b - bar(0)) / 8));
+    }
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   };
   auto warp_wait_cluster = [&](uint32_t b, uint32_t parity) -> bool {
     bool ok = true;
-    if (lane == 0) ok = mbar_wait_or_abort<true>(b, parity, lim, abort_flag, &timed_out);
+    if (lane == 0) {
+      ok = mbar_wait_or_abort<true>(b, parity, lim, abort_flag, &timed_out);
+      if (!ok && timed_out) MLA_SITE(1000 + warp * 100 + (int)((b - bar(0)) / 8));
+    }
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   };
 
@@ -259,7 +281,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     if (lane == 0) {
       TileIter it;
       it.init(p.seq_lens, p.max_blocks, b_first, blk_first);
-      const uint32_t tx = rank == 0 ? 5 * kBoxBytes : 4 * kBoxBytes;
+      const uint32_t tx = kStageBytes;
       int k = 0;
       for (; k < ntiles; ++k) {
         if (*abort_flag) break;
@@ -282,7 +304,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         const int y = pb * kTok;
         for (int c = 0; c < 4; ++c)
           tma_load_2d(dst + c * kBoxBytes, &tm_lat, (int)(rank * 4 + c) * 64, y, fb);
-        if (rank == 0) tma_load_2d(dst + 4 * kBoxBytes, &tm_rope, 0, y, fb);
+        tma_load_2d(dst + 4 * kBoxBytes, &tm_rope, (int)rank * 32, y, fb);
         if (k + 1 < ntiles) it.next();
       }
       // every issued load must land before the CTA may exit
@@ -302,8 +324,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     // the next score tile (lane 0 probes, the warp follows its decision).
     const uint32_t idS = idesc_bf16_f32(128, 64, false, false);
     const uint32_t idO = idesc_bf16_f32(128, 256, false, true);
-    const int nK = rank == 0 ? 20 : 16;     // 16-wide K steps of the partial score
-    const int nbox = rank == 0 ? 5 : 4;
+    const int nbox = 5;                     // boxes a ragged tile zero-fills (4 latent + RoPE)
     TileIter its, ito;
     its.init(p.seq_lens, p.max_blocks, b_first, blk_first);
     ito.init(p.seq_lens, p.max_blocks, b_first, blk_first);
@@ -312,6 +333,35 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     bool ok = true;
     while (ko < ntiles) {
       bool did = false;
+      // O(ko) first: it frees a P buffer and a stage
+      if (ko < ks) {
+        const bool first = (ko == 0) || (ito.blk == 0);
+        const bool last = (ko == ntiles - 1) || (ito.blk == ito.nb - 1);
+        bool ready = true;
+        if (lane == 0)
+          ready = (!(first && seg_o > 0) || mbar_test_wait(bar(BAR_O_FREE), (seg_o - 1) & 1)) &&
+                  mbar_test_wait(bar(BAR_P_FULL + (ko & 1)), (ko >> 1) & 1);
+        if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) {
+          tc_fence_after();
+          if (lane == 0) {
+            MLA_TR(ko, 2);
+            const uint32_t stage = sbase + kOffStages + (ko % kStages) * kStageBytes;
+            const uint32_t pcol = kColP + 32 * (ko & 1);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint64_t bd = smem_desc(stage + c * 2048, kBoxBytes, 1024, kSwizzle128B);
+              mma_ts(tmem + kColO, tmem + pcol + 8 * c, bd, idO, (first && c == 0) ? 0u : 1u);
+            }
+            mma_commit(bar(BAR_O_DONE + (ko & 1)));
+            mma_commit(bar(BAR_KV_EMPTY + (ko % kStages)));
+          }
+          __syncwarp();
+          if (last) ++seg_o;
+          if (ko + 1 < ntiles) ito.next();
+          ++ko;
+          did = true;
+        }
+      }
       if (ks < ntiles) {
         const int st = ks % kStages;
         const bool first = (ks == 0) || (its.blk == 0);
@@ -327,11 +377,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             // slots past the sequence end: zero them so that P = 0 meets finite values
             uint8_t* sp = smem + kOffStages + st * kStageBytes;
             const int nrow = kTok - n_valid;
-            for (int e = lane; e < nbox * nrow * 8; e += 32) {
+            for (int e = lane; e < 4 * nrow * 8; e += 32) {
               const int box = e / (nrow * 8), rr = (e / 8) % nrow, ch = e % 8;
               *reinterpret_cast<uint4*>(sp + box * kBoxBytes + (n_valid + rr) * 128 + ch * 16) =
                   make_uint4(0, 0, 0, 0);
             }
+            for (int e = lane; e < nrow * 4; e += 32)
+              *reinterpret_cast<uint4*>(sp + 4 * kBoxBytes + (n_valid + e / 4) * 64 + (e % 4) * 16) =
+                  make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
           }
           __syncwarp();
@@ -339,10 +392,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           if (lane == 0) {
             MLA_TR(ks, 1);
             const uint32_t stage = sbase + kOffStages + st * kStageBytes;
-            for (int kk = 0; kk < nK; ++kk) {
+            for (int kk = 0; kk < 16; ++kk) {
               const uint64_t bd = smem_desc(stage + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16,
                                             1024, kSwizzle128B);
               mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bd, idS, kk > 0 ? 1u : 0u);
+            }
+            // this CTA's 32 RoPE dims: query slice and keys in shared memory (64-byte swizzle)
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint64_t ad = smem_desc(sbase + kOffQRope + kk * 32, 16, 512, kSwizzle64B);
+              const uint64_t bd = smem_desc(stage + 4 * kBoxBytes + kk * 32, 16, 512, kSwizzle64B);
+              mma_ss(tmem + kColS, ad, bd, idS, 1u);
             }
             mma_commit(bar(BAR_S_FULL + (ks & 1)));
             if (last) mma_commit(bar(BAR_Q_FREE));
@@ -354,33 +413,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           did = true;
         }
       }
-      if (ko < ks) {
-        const bool first = (ko == 0) || (ito.blk == 0);
-        const bool last = (ko == ntiles - 1) || (ito.blk == ito.nb - 1);
-        bool ready = true;
-        if (lane == 0)
-          ready = (!(first && seg_o > 0) || mbar_test_wait(bar(BAR_O_FREE), (seg_o - 1) & 1)) &&
-                  mbar_test_wait(bar(BAR_P_FULL + (ko & 1)), (ko >> 1) & 1);
-        if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) {
-          tc_fence_after();
-          if (lane == 0) {
-            MLA_TR(ko, 2);
-            const uint32_t stage = sbase + kOffStages + (ko % kStages) * kStageBytes;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint64_t bd = smem_desc(stage + c * 2048, kBoxBytes, 1024, kSwizzle128B);
-              mma_ts(tmem + kColO, tmem + kColP + 8 * c, bd, idO, (first && c == 0) ? 0u : 1u);
-            }
-            mma_commit(bar(BAR_O_DONE + (ko & 1)));
-            mma_commit(bar(BAR_KV_EMPTY + (ko % kStages)));
-          }
-          __syncwarp();
-          if (last) ++seg_o;
-          if (ko + 1 < ntiles) ito.next();
-          ++ko;
-          did = true;
-        }
-      }
       if (did) {
         idle_since = clock64();
       } else {
@@ -388,6 +420,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (clock64() - idle_since > lim) {
           timed_out = true;
           ok = false;
+          if (lane == 0) MLA_SITE(2000 + ks * 0 + (ko < 1000 ? ko : 999));
           break;
         }
       }
@@ -424,11 +457,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     // [0, 256) ++ [512, 576), CTA 1 dims [256, 512); 16-column chunks (32
     // dims) are split between the two groups.
     auto load_q = [&](int b) {
+      if (group_lead && g == 0) {
+        // RoPE dims [512 + 32 rank, +32) of the 128 query rows of sequence b
+        mbar_arrive_expect_tx(bar(BAR_Q_READY), kQRopeBytes);
+        tma_load_2d(sbase + kOffQRope, &tm_q, 512 + 32 * (int)rank, b * p.h, bar(BAR_Q_READY));
+      }
       const uint4* q = reinterpret_cast<const uint4*>(p.q_cat + ((int64_t)b * p.h + (live ? row : 0)) * 576);
-      const int nchunk = rank == 0 ? 10 : 8;
-      const int c0 = g * (nchunk / 2), c1 = c0 + nchunk / 2;
-      for (int c = c0; c < c1; ++c) {
-        const int dim0 = rank == 0 ? (c < 8 ? 32 * c : 512 + 32 * (c - 8)) : 256 + 32 * c;
+      for (int c = 4 * g; c < 4 * g + 4; ++c) {
+        const int dim0 = 256 * (int)rank + 32 * c;
         uint32_t w[16];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -541,16 +577,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         }
         l_g += psum;
 
-        // ---- the single TMEM P buffer was read by the P.C MMA of tile k-1; wait
-        // for it (first for tile k-2 on this group's own barrier, so that the
-        // wait on the other group's barrier cannot alias an older phase)
+        // ---- P buffer (k & 1) was read by the P.C MMA of tile k-2; waiting for it
+        // also makes O(k-3) complete, so the rescale's wait on the other group's
+        // barrier below cannot alias an older phase
         if (k >= 2 && !warp_wait(bar(BAR_O_DONE + (k & 1)), ((k - 2) >> 1) & 1)) { ok = false; break; }
-        if (k >= 1 && !warp_wait(bar(BAR_O_DONE + ((k - 1) & 1)), ((k - 1) >> 1) & 1)) { ok = false; break; }
         if (group_lead) MLA_TR(k, 7);
-        tc_fence_after();
 
         // ---- rescale O between P(k-1) C and P(k) C (rare)
         if (__any_sync(0xffffffffu, resc)) {
+          const int kp = k - 1;
+          if (!warp_wait(bar(BAR_O_DONE + (kp & 1)), (kp >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
           const float alpha = resc ? exp2f(m_prev - m_k) : 1.0f;
           for (int c = 0; c < 16; ++c) {
             uint32_t v[16];
@@ -561,8 +598,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             tmem_st16(tl + kColO + 16 * c, v);
           }
         }
-        tmem_st16(tl + kColP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(tl + kColP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        tc_fence_after();
+        const uint32_t pcol = kColP + 32 * (k & 1);
+        tmem_st16(tl + pcol, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(tl + pcol + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -639,18 +678,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() { return tensor_map_encoder(); }
 
-// 2-D bf16 view [rows, cols] with the given row pitch, 64 x 64 boxes, 128-byte swizzle.
+// 2-D bf16 view [rows, cols] with the given row pitch; box_cols x box_rows boxes,
+// 128-byte swizzle for 64-column boxes and 64-byte swizzle for 32-column boxes.
 bool make_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
-               uint64_t row_pitch_bytes) {
+               uint64_t row_pitch_bytes, uint32_t box_cols, uint32_t box_rows) {
   auto fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_pitch_bytes};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw =
+      box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -702,10 +744,11 @@ cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                              int B, int h, int num_parts, float scale, float* o_part,
                              float* lse_part, int32_t* status, cudaStream_t s) {
-  CUtensorMap tm_lat, tm_rope;
+  CUtensorMap tm_lat, tm_rope, tm_q;
   const uint64_t rows = (uint64_t)kv.num_blocks * kv.block_size;
-  if (!make_tmap(&tm_lat, kv.latent, 512, rows, (uint64_t)kv.latent_stride * 2) ||
-      !make_tmap(&tm_rope, kv.rope, 64, rows, (uint64_t)kv.rope_stride * 2))
+  if (!make_tmap(&tm_lat, kv.latent, 512, rows, (uint64_t)kv.latent_stride * 2, 64, 64) ||
+      !make_tmap(&tm_rope, kv.rope, 64, rows, (uint64_t)kv.rope_stride * 2, 32, 64) ||
+      !make_tmap(&tm_q, q_cat, 576, (uint64_t)B * h, 576 * 2, 32, 128))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
@@ -729,7 +772,7 @@ cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.wait_limit = 4000000000LL;  // about 2 s of SM clock
   dim3 grid(2 * num_parts);
-  decode_tc_kernel<<<grid, kThreads, kSmemAlloc, s>>>(tm_lat, tm_rope, prm);
+  decode_tc_kernel<<<grid, kThreads, kSmemAlloc, s>>>(tm_lat, tm_rope, tm_q, prm);
   return cudaGetLastError();
 }
 

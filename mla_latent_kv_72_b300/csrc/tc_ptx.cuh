@@ -278,6 +278,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 
 constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzle64B = 4;
 
 // Instruction descriptor of kind::f16 with bf16 A and B, float32 accumulator.
 // a_mn / b_mn select MN-major operands.
