@@ -55,18 +55,24 @@ using namespace tc;
 
 constexpr int kTok = 64;                    // tokens per tile (= cache block)
 constexpr int kStages = 4;
+constexpr int kPrefetch = 6;                // tiles prefetched into L2 beyond the stages
+constexpr int kGroups = 2;                  // softmax warpgroups (tile k goes to group k % kGroups)
 constexpr int kBoxBytes = 64 * 128;         // 64 rows x 64 bf16, 128-byte swizzle
 constexpr int kRopeBoxBytes = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
 constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // 4 latent boxes + half the RoPE dims
 constexpr int kQRopeBytes = 128 * 64;       // query RoPE slice: 128 heads x 32 bf16
-constexpr int kRecvBytes = 128 * 64 * 4;    // partial S of the peer, float32
+// partial S of the peer: 64 scores per row, each the top 24 bits of a float32
+// (sign, exponent, 15 mantissa bits) with a use tag in the low byte, so that
+// the receiver can tell fresh values from the previous use's by looking at them
+constexpr int kXChunks = 16;                // 16-byte chunks per row
+constexpr int kRecvBytes = 128 * kXChunks * 16;
 
 constexpr int kOffStages = 0;
 constexpr int kOffRecv = kOffStages + kStages * kStageBytes;
-constexpr int kOffQRope = kOffRecv + 2 * kRecvBytes;    // 1024-aligned
+constexpr int kOffQRope = kOffRecv + kGroups * kRecvBytes;  // 1024-aligned
 constexpr int kOffMpub = kOffQRope + kQRopeBytes;       // [2][128] float
-constexpr int kOffLstate = kOffMpub + 2 * 128 * 4;      // [2 seg][2 group][128] float2
-constexpr int kOffBar = kOffLstate + 2 * 2 * 128 * 8;
+constexpr int kOffLstate = kOffMpub + 2 * 128 * 4;      // [2 seg][kGroups][128] float2
+constexpr int kOffBar = kOffLstate + 2 * kGroups * 128 * 8;
 constexpr int kNumBars = 32;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64;
@@ -79,7 +85,7 @@ constexpr uint32_t kColQ = 320;   // latent query slice (bf16 pairs), 128 column
 constexpr uint32_t kColP = 448;   // [2] P (bf16 pairs, 32 columns each), A of the P.C MMA
 constexpr uint32_t kTmemCols = 512;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 64 + 128 * kGroups;
 constexpr float kTau = 8.0f;  // lazy rescale threshold (log2 units): P stays <= 2^8
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -87,15 +93,15 @@ constexpr float kLn2 = 0.69314718055994530942f;
 enum {
   BAR_KV_FULL = 0,                      // [kStages] TMA -> MMA
   BAR_KV_EMPTY = BAR_KV_FULL + kStages, // [kStages] MMA (commit after P.C) -> TMA
-  BAR_S_FULL = BAR_KV_EMPTY + kStages,  // [2] MMA -> softmax group (k & 1); one barrier per
-                                        //     group so that a group's parity waits never
-                                        //     alias the other group's phases
-  BAR_S_EMPTY = BAR_S_FULL + 2,         // softmax (4 warps) -> MMA
-  BAR_P_FULL = BAR_S_EMPTY + 1,         // [2] softmax (4 warps) -> MMA
-  BAR_O_DONE = BAR_P_FULL + 2,          // [2] MMA -> softmax (P buffer free, O final)
-  BAR_RECV_FULL = BAR_O_DONE + 2,       // [2] peer's 4 warps have written their partial scores
-  BAR_PEER_FREE = BAR_RECV_FULL + 2,    // [2] peer's 4 warps have read what we sent
-  BAR_MREADY = BAR_PEER_FREE + 2,       // [2] running maximum of a tile published (4 warps)
+  BAR_S_FULL = BAR_KV_EMPTY + kStages,  // [kGroups] MMA -> softmax group k % kGroups; one
+                                        //     barrier per group so that a group's parity
+                                        //     waits never alias another group's phases
+  BAR_S_EMPTY = BAR_S_FULL + kGroups,   // softmax (4 warps) -> MMA
+  BAR_P_FULL = BAR_S_EMPTY + 1,         // [2] softmax (4 warps) -> MMA, by P buffer k & 1
+  BAR_O_DONE = BAR_P_FULL + 2,          // [4] MMA -> softmax, by k & 3 (P buffer free, O final);
+                                        //     four so that no waiter can be two phases off
+  BAR_PEER_FREE = BAR_O_DONE + 4,       // [kGroups] peer's 4 warps have read what we sent
+  BAR_MREADY = BAR_PEER_FREE + kGroups, // [2] running maximum of tile k published, by k & 1
   BAR_Q_FREE = BAR_MREADY + 2,          // MMA: last score MMA of a segment done
   BAR_Q_READY = BAR_Q_FREE + 1,         // softmax (8 warps) + TMA of the RoPE query slice
   BAR_O_FREE = BAR_Q_READY + 1,         // softmax (8 warps): O of a segment read out
@@ -117,6 +123,14 @@ struct TcParams {
   long long wait_limit;
 };
 
+// 2^x on the SFU (subnormal results flush to zero: P values that small do not
+// change the sums)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -126,7 +140,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // -DMLA_TRACE; the product build has none of it).
 #ifdef MLA_TRACE
 constexpr int kTraceTiles = 128;
-constexpr int kTraceEv = 12;
+constexpr int kTraceEv = 16;
 __device__ unsigned long long* g_trace = nullptr;
 #define MLA_TR(k, ev)                                                                   \
   do {                                                                                  \
@@ -202,18 +216,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       mbar_init(bar(BAR_KV_EMPTY + s), 1);
     }
     mbar_init(bar(BAR_S_EMPTY), 4);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kGroups; ++i) {
       mbar_init(bar(BAR_S_FULL + i), 1);
-      mbar_init(bar(BAR_P_FULL + i), 4);
-      mbar_init(bar(BAR_O_DONE + i), 1);
-      mbar_init(bar(BAR_RECV_FULL + i), 4);
       mbar_init(bar(BAR_PEER_FREE + i), 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(BAR_P_FULL + i), 4);
       mbar_init(bar(BAR_MREADY + i), 4);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(bar(BAR_O_DONE + i), 1);
     mbar_init(bar(BAR_Q_FREE), 1);
-    mbar_init(bar(BAR_Q_READY), 9);
-    mbar_init(bar(BAR_O_FREE), 8);
-    mbar_init(bar(BAR_SEG), 8);
+    mbar_init(bar(BAR_Q_READY), 4 * kGroups + 1);
+    mbar_init(bar(BAR_O_FREE), 4 * kGroups);
+    mbar_init(bar(BAR_SEG), 4 * kGroups);
     mbar_init(bar(BAR_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -246,6 +261,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
+  // exchange buffers start with tag 0, which no use carries
+  for (int i = threadIdx.x; i < kGroups * kRecvBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + kOffRecv)[i] = make_uint4(0, 0, 0, 0);
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated, part known
   tc_fence_after();
@@ -282,8 +300,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       TileIter it;
       it.init(p.seq_lens, p.max_blocks, b_first, blk_first);
       const uint32_t tx = kStageBytes;
+      // L2 prefetch runs kPrefetch tiles ahead of the loads, so that a stage
+      // freed late (after its P.C MMA) refills from L2 rather than HBM
+      TileIter pf;
+      pf.init(p.seq_lens, p.max_blocks, b_first, blk_first);
+      int kp = 0;
+      auto prefetch_upto = [&](int kend) {
+        for (; kp < kend && kp < ntiles; ++kp) {
+          const int pb = p.block_table[(int64_t)pf.b * p.max_blocks + pf.blk];
+          if (pb >= 0 && pb < p.num_blocks) {
+            for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tm_lat, (int)(rank * 4 + c) * 64, pb * kTok);
+            tma_prefetch_2d(&tm_rope, (int)rank * 32, pb * kTok);
+          }
+          if (kp + 1 < ntiles) pf.next();
+        }
+      };
       int k = 0;
       for (; k < ntiles; ++k) {
+        prefetch_upto(k + kStages + kPrefetch);
         if (*abort_flag) break;
         const int st = k % kStages;
         if (k >= kStages &&
@@ -331,34 +365,41 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     int ks = 0, ko = 0, seg_s = 0, seg_o = 0;
     long long idle_since = clock64();
     bool ok = true;
+    // lane 0: issue O(ko) if its P is ready (state is advanced by advance_o on all lanes)
+    auto try_issue_o_lane0 = [&]() -> bool {
+      if (ko >= ks) return false;
+      const bool first = (ko == 0) || (ito.blk == 0);
+      const bool ready =
+          (!(first && seg_o > 0) || mbar_test_wait(bar(BAR_O_FREE), (seg_o - 1) & 1)) &&
+          mbar_test_wait(bar(BAR_P_FULL + (ko & 1)), (ko >> 1) & 1);
+      if (!ready) return false;
+      tc_fence_after();
+      MLA_TR(ko, 2);
+      const uint32_t stage = sbase + kOffStages + (ko % kStages) * kStageBytes;
+      const uint32_t pcol = kColP + 32 * (ko & 1);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint64_t bd = smem_desc(stage + c * 2048, kBoxBytes, 1024, kSwizzle128B);
+        mma_ts(tmem + kColO, tmem + pcol + 8 * c, bd, idO, (first && c == 0) ? 0u : 1u);
+      }
+      mma_commit(bar(BAR_O_DONE + (ko & 3)));
+      mma_commit(bar(BAR_KV_EMPTY + (ko % kStages)));
+      return true;
+    };
+    auto advance_o = [&]() {
+      const bool last = (ko == ntiles - 1) || (ito.blk == ito.nb - 1);
+      if (last) ++seg_o;
+      if (ko + 1 < ntiles) ito.next();
+      ++ko;
+    };
     while (ko < ntiles) {
       bool did = false;
       // O(ko) first: it frees a P buffer and a stage
-      if (ko < ks) {
-        const bool first = (ko == 0) || (ito.blk == 0);
-        const bool last = (ko == ntiles - 1) || (ito.blk == ito.nb - 1);
-        bool ready = true;
-        if (lane == 0)
-          ready = (!(first && seg_o > 0) || mbar_test_wait(bar(BAR_O_FREE), (seg_o - 1) & 1)) &&
-                  mbar_test_wait(bar(BAR_P_FULL + (ko & 1)), (ko >> 1) & 1);
-        if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) {
-          tc_fence_after();
-          if (lane == 0) {
-            MLA_TR(ko, 2);
-            const uint32_t stage = sbase + kOffStages + (ko % kStages) * kStageBytes;
-            const uint32_t pcol = kColP + 32 * (ko & 1);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint64_t bd = smem_desc(stage + c * 2048, kBoxBytes, 1024, kSwizzle128B);
-              mma_ts(tmem + kColO, tmem + pcol + 8 * c, bd, idO, (first && c == 0) ? 0u : 1u);
-            }
-            mma_commit(bar(BAR_O_DONE + (ko & 1)));
-            mma_commit(bar(BAR_KV_EMPTY + (ko % kStages)));
-          }
-          __syncwarp();
-          if (last) ++seg_o;
-          if (ko + 1 < ntiles) ito.next();
-          ++ko;
+      {
+        bool issued = false;
+        if (lane == 0) issued = try_issue_o_lane0();
+        if (__shfl_sync(0xffffffffu, issued ? 1 : 0, 0)) {
+          advance_o();
           did = true;
         }
       }
@@ -367,10 +408,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         const bool first = (ks == 0) || (its.blk == 0);
         const bool last = (ks == ntiles - 1) || (its.blk == its.nb - 1);
         bool ready = true;
-        if (lane == 0)
-          ready = (!first || mbar_test_wait(bar(BAR_Q_READY), seg_s & 1)) &&
-                  mbar_test_wait(bar(BAR_KV_FULL + st), (ks / kStages) & 1) &&
-                  (ks == 0 || mbar_test_wait(bar(BAR_S_EMPTY), (ks - 1) & 1));
+        if (lane == 0) {
+          const bool q_ok = !first || mbar_test_wait(bar(BAR_Q_READY), seg_s & 1);
+          const bool kv_ok = mbar_test_wait(bar(BAR_KV_FULL + st), (ks / kStages) & 1);
+          const bool s_ok = ks == 0 || mbar_test_wait(bar(BAR_S_EMPTY), (ks - 1) & 1);
+#ifdef MLA_TRACE
+          if (kv_ok && g_trace != nullptr && part < 2 && ks < kTraceTiles &&
+              g_trace[((part * 2 + rank) * kTraceTiles + ks) * kTraceEv + 12] == 0)
+            MLA_TR(ks, 12);
+          if (s_ok && g_trace != nullptr && part < 2 && ks < kTraceTiles &&
+              g_trace[((part * 2 + rank) * kTraceTiles + ks) * kTraceEv + 13] == 0)
+            MLA_TR(ks, 13);
+#endif
+          ready = q_ok && kv_ok && s_ok;
+        }
         if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) {
           const int n_valid = its.valid();
           if (n_valid < kTok) {
@@ -389,6 +440,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           }
           __syncwarp();
           tc_fence_after();
+          bool o_issued_inside = false;
           if (lane == 0) {
             MLA_TR(ks, 1);
             const uint32_t stage = sbase + kOffStages + st * kStageBytes;
@@ -396,6 +448,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
               const uint64_t bd = smem_desc(stage + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16,
                                             1024, kSwizzle128B);
               mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bd, idS, kk > 0 ? 1u : 0u);
+              // a P.C MMA that became ready meanwhile goes in between (the two
+              // accumulators are independent), so its stage is freed sooner
+              if (kk == 7 && try_issue_o_lane0()) o_issued_inside = true;
             }
             // this CTA's 32 RoPE dims: query slice and keys in shared memory (64-byte swizzle)
             for (int kk = 0; kk < 2; ++kk) {
@@ -403,9 +458,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
               const uint64_t bd = smem_desc(stage + 4 * kBoxBytes + kk * 32, 16, 512, kSwizzle64B);
               mma_ss(tmem + kColS, ad, bd, idS, 1u);
             }
-            mma_commit(bar(BAR_S_FULL + (ks & 1)));
+            mma_commit(bar(BAR_S_FULL + (ks % kGroups)));
             if (last) mma_commit(bar(BAR_Q_FREE));
           }
+          if (__shfl_sync(0xffffffffu, o_issued_inside ? 1 : 0, 0)) advance_o();
           __syncwarp();
           if (last) ++seg_s;
           if (ks + 1 < ntiles) its.next();
@@ -416,6 +472,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       if (did) {
         idle_since = clock64();
       } else {
+        // back off: a spinning MMA warp would take issue slots from the
+        // softmax warps that share its SM sub-partition
+        __nanosleep(64);
         if (*abort_flag) { ok = false; break; }
         if (clock64() - idle_since > lim) {
           timed_out = true;
@@ -436,7 +495,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     __syncwarp();
   } else if (b_first >= 0 && ntiles > 0 && warp >= 2) {
     // ------------------------------------------------------------ softmax groups
-    const int g = (warp - 2) >> 2;            // group: tiles k with (k & 1) == g
+    const int g = (warp - 2) >> 2;            // group: tiles k with k % kGroups == g
     const int sub = warp & 3;                 // TMEM sub-partition of this warp
     const int row = sub * 32 + lane;          // head
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
@@ -445,12 +504,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     float* mpub = reinterpret_cast<float*>(smem + kOffMpub);
     float2* lstate = reinterpret_cast<float2*>(smem + kOffLstate);
     // exchange buffers: chunk c (16 B) of row sub * 32 + lane at
-    // sub * 8192 + c * 512 + lane * 16, so that a warp's stores and loads are
-    // contiguous 512-byte runs
-    const uint32_t xoff = (uint32_t)(sub * 8192 + lane * 16);
+    // (sub * kXChunks + c) * 512 + lane * 16, so that a warp's stores and loads
+    // are contiguous 512-byte runs
+    const uint32_t xoff = (uint32_t)(sub * kXChunks * 512 + lane * 16);
     const uint8_t* my_recv = smem + kOffRecv + g * kRecvBytes + xoff;
+    const uint32_t my_recv_u32 = sbase + kOffRecv + g * kRecvBytes + xoff;
     const uint32_t peer_recv = mapa(sbase + kOffRecv + g * kRecvBytes + xoff, peer);
-    const uint32_t peer_recv_full = mapa(bar(BAR_RECV_FULL + g), peer);
     const uint32_t peer_free = mapa(bar(BAR_PEER_FREE + g), peer);
 
     // query slice of sequence b -> TMEM (A operand).  CTA 0 holds dims
@@ -463,7 +522,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         tma_load_2d(sbase + kOffQRope, &tm_q, 512 + 32 * (int)rank, b * p.h, bar(BAR_Q_READY));
       }
       const uint4* q = reinterpret_cast<const uint4*>(p.q_cat + ((int64_t)b * p.h + (live ? row : 0)) * 576);
-      for (int c = 4 * g; c < 4 * g + 4; ++c) {
+      for (int c = (8 * g) / kGroups; c < (8 * (g + 1)) / kGroups; ++c) {
         const int dim0 = 256 * (int)rank + 32 * c;
         uint32_t w[16];
 #pragma unroll
@@ -493,8 +552,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       const bool first = (k == 0) || (it.blk == 0);
       const bool last = (k == ntiles - 1) || (it.blk == it.nb - 1);
 
-      if ((k & 1) == g) {
-        const int u = k >> 1;  // use index of this group's exchange buffers
+      if (k % kGroups == g) {
+        const int u = k / kGroups;  // use index of this group's exchange buffers
         const int n_valid = it.valid();
         // ---- partial scores of this CTA
         if (!warp_wait(bar(BAR_S_FULL + g), u & 1)) { ok = false; break; }
@@ -506,40 +565,80 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         tmem_ld16(tl + kColS + 32, *reinterpret_cast<uint32_t(*)[16]>(&r[32]));
         tmem_ld16(tl + kColS + 48, *reinterpret_cast<uint32_t(*)[16]>(&r[48]));
         tmem_wait_ld();
+        if (group_lead) MLA_TR(k, 9);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_S_EMPTY));
 
         // ---- exchange with the peer CTA
-        if (u >= 1 && !warp_wait_cluster(bar(BAR_PEER_FREE + g), (u - 1) & 1)) { ok = false; break; }
+        // (no data comes back with this signal, so a CTA-scope wait suffices)
+        if (u >= 1 && !warp_wait(bar(BAR_PEER_FREE + g), (u - 1) & 1)) { ok = false; break; }
+        if (group_lead) MLA_TR(k, 10);
+        // both CTAs keep only the top 24 bits of each partial (their own and
+        // the peer's), so the two sums stay bit-identical; the freed low byte
+        // of every value sent carries the use tag (1..255)
+        const uint32_t tag = (uint32_t)(u % 255) + 1u;
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_cluster_v4(peer_recv + c * 512, __uint_as_float(r[4 * c]),
-                        __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
-                        __uint_as_float(r[4 * c + 3]));
-        // one release arrive per warp publishes the warp's 32 rows to the peer
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(peer_recv_full);
+        for (int i = 0; i < 64; ++i) r[i] &= 0xFFFFFF00u;
+#pragma unroll
+        for (int c = 0; c < kXChunks; ++c)
+          st_cluster_v4(peer_recv + c * 512, __uint_as_float(r[4 * c] | tag),
+                        __uint_as_float(r[4 * c + 1] | tag), __uint_as_float(r[4 * c + 2] | tag),
+                        __uint_as_float(r[4 * c + 3] | tag));
+        if (group_lead) MLA_TR(k, 11);
         if (group_lead) MLA_TR(k, 4);
-        if (!warp_wait_cluster(bar(BAR_RECV_FULL + g), u & 1)) { ok = false; break; }
+        // poll the local buffer until all 64 values of this row carry the tag
+        // (each 4-byte value is written atomically, so a tagged value is whole)
+        {
+          const long long t0 = clock64();
+          bool got = false;
+          while (true) {
+            bool mine = true;
+#pragma unroll
+            for (int c = 0; c < kXChunks; ++c) {
+              uint32_t v0, v1, v2, v3;
+              asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                           : "r"(my_recv_u32 + c * 512)
+                           : "memory");
+              mine &= ((v0 & 0xFFu) == tag) & ((v1 & 0xFFu) == tag) & ((v2 & 0xFFu) == tag) &
+                      ((v3 & 0xFFu) == tag);
+            }
+            if (__all_sync(0xffffffffu, mine)) { got = true; break; }
+            if (*abort_flag) break;
+            if (clock64() - t0 > lim) {
+              timed_out = true;
+              if (lane == 0) MLA_SITE(3000 + warp);
+              break;
+            }
+          }
+          if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        }
         if (group_lead) MLA_TR(k, 5);
         // full score (log2 domain) in place: r <- (own partial + peer's) * scale
         float mt = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 v = *reinterpret_cast<const float4*>(my_recv + c * 512);
-          const float vv[4] = {v.x, v.y, v.z, v.w};
+        for (int c = 0; c < kXChunks; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(my_recv + c * 512);
+          const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int kk = 4 * c + e;
-            const float xs = kk < n_valid ? (__uint_as_float(r[kk]) + vv[e]) * p.scale_log2
-                                          : -INFINITY;
+            const float xs =
+                (__uint_as_float(r[kk]) + __uint_as_float(vv[e] & 0xFFFFFF00u)) * p.scale_log2;
             r[kk] = __float_as_uint(xs);
-            mt = fmaxf(mt, xs);
           }
         }
+        // the buffer may be refilled: tell the peer (the values are consumed)
         __syncwarp();
         if (lane == 0) mbar_arrive_remote_relaxed(peer_free);
+        if (n_valid < kTok) {  // ragged last block: slots past the end get -inf
+#pragma unroll
+          for (int kk = 0; kk < 64; ++kk)
+            if (kk >= n_valid) r[kk] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 64; ++kk) mt = fmaxf(mt, __uint_as_float(r[kk]));
 
         // ---- running maximum, handed over from the previous tile's group
         float m_prev = -INFINITY;
@@ -565,28 +664,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           m_g = m_k;
         }
 
-        // ---- P (bf16 pairs) in registers first, overlapping the P.C MMA of tile k-1
-        uint32_t pk[32];
+        // ---- P (bf16 pairs) in registers first, packed in place into r[0..31]
         float psum = 0.f;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = exp2f(__uint_as_float(r[2 * e]) - m_k);
-          const float p1 = exp2f(__uint_as_float(r[2 * e + 1]) - m_k);
+          const float p0 = ex2(__uint_as_float(r[2 * e]) - m_k);
+          const float p1 = ex2(__uint_as_float(r[2 * e + 1]) - m_k);
           psum += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          r[e] = pack_bf16x2(p0, p1);
         }
         l_g += psum;
 
         // ---- P buffer (k & 1) was read by the P.C MMA of tile k-2; waiting for it
         // also makes O(k-3) complete, so the rescale's wait on the other group's
         // barrier below cannot alias an older phase
-        if (k >= 2 && !warp_wait(bar(BAR_O_DONE + (k & 1)), ((k - 2) >> 1) & 1)) { ok = false; break; }
+        if (k >= 2 && !warp_wait(bar(BAR_O_DONE + ((k - 2) & 3)), ((k - 2) >> 2) & 1)) { ok = false; break; }
         if (group_lead) MLA_TR(k, 7);
 
         // ---- rescale O between P(k-1) C and P(k) C (rare)
         if (__any_sync(0xffffffffu, resc)) {
           const int kp = k - 1;
-          if (!warp_wait(bar(BAR_O_DONE + (kp & 1)), (kp >> 1) & 1)) { ok = false; break; }
+          if (!warp_wait(bar(BAR_O_DONE + (kp & 3)), (kp >> 2) & 1)) { ok = false; break; }
           tc_fence_after();
           const float alpha = resc ? exp2f(m_prev - m_k) : 1.0f;
           for (int c = 0; c < 16; ++c) {
@@ -600,8 +698,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         }
         tc_fence_after();
         const uint32_t pcol = kColP + 32 * (k & 1);
-        tmem_st16(tl + pcol, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(tl + pcol + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        tmem_st16(tl + pcol, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+        tmem_st16(tl + pcol + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -611,15 +709,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
       if (last) {
         // ---- end of a segment: both groups
-        float2* ls = lstate + (seg & 1) * 256;
+        float2* ls = lstate + (seg & 1) * (kGroups * 128);
         ls[g * 128 + row] = make_float2(m_g, l_g);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_SEG));
         if (!warp_wait(bar(BAR_SEG), seg & 1)) { ok = false; break; }
-        const float2 o = ls[(1 - g) * 128 + row];
-        const float M = fmaxf(m_g, o.x);
-        const float l = (m_g != -INFINITY ? l_g * exp2f(m_g - M) : 0.f) +
-                        (o.x != -INFINITY ? o.y * exp2f(o.x - M) : 0.f);
+        float M = -INFINITY;
+#pragma unroll
+        for (int gg = 0; gg < kGroups; ++gg) M = fmaxf(M, ls[gg * 128 + row].x);
+        float l = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < kGroups; ++gg) {
+          const float2 o = ls[gg * 128 + row];
+          if (o.x != -INFINITY) l += o.y * exp2f(o.x - M);
+        }
         const int b = it.b;
         // query of the next segment first: the MMA warp issues the last P.C
         // of this segment only after the next segment's first score MMA
@@ -631,14 +734,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           load_q(nx.b);
         }
         // epilogue: O_r / l -> o_part slot (part + b); this group's 128 columns
-        if (!warp_wait(bar(BAR_O_DONE + (k & 1)), (k >> 1) & 1)) { ok = false; break; }
+        if (!warp_wait(bar(BAR_O_DONE + (k & 3)), (k >> 2) & 1)) { ok = false; break; }
         tc_fence_after();
         const int64_t slot = (int64_t)part + b;
-        float* orow = p.o_part + (slot * p.h + row) * 512 + rank * 256 + g * 128;
+        float* orow = p.o_part + (slot * p.h + row) * 512 + rank * 256;
         const float inv = 1.0f / l;
-        for (int c = 0; c < 8; ++c) {
+        for (int c = (16 * g) / kGroups; c < (16 * (g + 1)) / kGroups; ++c) {
           uint32_t v[16];
-          tmem_ld16(tl + kColO + g * 128 + 16 * c, v);
+          tmem_ld16(tl + kColO + 16 * c, v);
           tmem_wait_ld();
           if (live) {
 #pragma unroll
