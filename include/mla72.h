@@ -183,9 +183,11 @@ int mla_decode_num_partials(int B, int num_parts);
  *   lse_part   [mla_decode_num_partials(B, num_parts), h] float32 (output)
  *   dev_status int32 device word, may be NULL (see conventions)
  *   flags      MLA_DECODE_AUTO or MLA_DECODE_FORCE_SIMT
- * Supported dtypes: (q, latent, rope) = (F32, F32, F32) and (BF16, FP8E4M3, BF16)
- * on the SIMT kernel; (BF16, BF16, BF16) on both kernels.  The tensor-core
- * kernel runs for BF16 caches with d_c = 512, d_r = 64, block_size = 64, h <= 128.
+ * Supported dtypes: (q, latent, rope) = (F32, F32, F32) on the SIMT kernel;
+ * (BF16, BF16, BF16) and (BF16, FP8E4M3, BF16) on both kernels.  The tensor-core
+ * kernel runs for d_c = 512, d_r = 64, block_size = 64, h <= 128; for an FP8
+ * latent it dequantises each code to bf16(e4m3 value x block scale) before
+ * the MMAs (relative rounding <= 2^-9 per element).
  * softmax_scale <= 0 selects 1/sqrt(d_nope + d_r) with d_nope = 128.
  */
 int mla_decode_fwd(const void* q_cat, int q_dtype, const mla_kv_cache* kv,

@@ -65,14 +65,14 @@ absorb_q_simt_kernel(const void* __restrict__ q_nope, const void* __restrict__ q
 
   // RoPE of the rotary query part: pair i of row (b, s) rotated by q_pos[b] * theta^(-2i/d_r).
   const int half = d_r / 2;
+  __shared__ double inv_freq[128];
+  for (int i = threadIdx.x; i < half; i += kThreads) inv_freq[i] = pow(theta, -2.0 * (double)i / (double)d_r);
+  __syncthreads();
   for (int i = threadIdx.x; i < nb * half; i += kThreads) {
     int bb = i / half, p = i % half;
     int b = b0 + bb;
-    double inv = pow(theta, -2.0 * (double)p / (double)d_r);
-    double ang = (double)q_pos[b] * inv;
-    double sd, cd;
-    sincos(ang, &sd, &cd);
-    float cs = (float)cd, sn = (float)sd;
+    float cs, sn;
+    rope_cos_sin((double)q_pos[b], inv_freq[p], &cs, &sn);
     int64_t ib = ((int64_t)b * h + s) * d_r;
     float x0 = load_as_f32(q_rope, dtype, ib + 2 * p);
     float x1 = load_as_f32(q_rope, dtype, ib + 2 * p + 1);

@@ -76,13 +76,14 @@ cache_fill_kernel(const void* __restrict__ c_kv, const void* __restrict__ k_rope
 
   // RoPE of the key at its position t: pair p rotated by t * theta^(-2p/d_r)
   const int half = d_r / 2;
+  __shared__ double inv_freq[128];
+  for (int i = threadIdx.x; i < half; i += kThreads) inv_freq[i] = pow(theta, -2.0 * (double)i / (double)d_r);
+  __syncthreads();
   for (int i = threadIdx.x; i < n * half; i += kThreads) {
     int r = i / half, p = i % half;
     int t = t0 + r;
-    double inv = pow(theta, -2.0 * (double)p / (double)d_r);
-    double sd, cd;
-    sincos((double)t * inv, &sd, &cd);
-    float cs = (float)cd, sn = (float)sd;
+    float cs, sn;
+    rope_cos_sin((double)t, inv_freq[p], &cs, &sn);
     float x0 = load_as_f32(k_rope, kv.rope_dtype, (src0 + r) * d_r + 2 * p);
     float x1 = load_as_f32(k_rope, kv.rope_dtype, (src0 + r) * d_r + 2 * p + 1);
     int64_t o = (dst0 + r) * kv.rope_stride + 2 * p;

@@ -12,24 +12,26 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kHeadsPerCta = 8;              // one warp per head
+constexpr int kThreads = 32 * kHeadsPerCta;
 constexpr int kMaxSplits = 1024;
 
-// grid: (h, B); block: 128 threads, each owning 4 consecutive latent columns per pass.
+// grid: (ceil(h / kHeadsPerCta), B); warp w merges head blockIdx.x * 8 + w of
+// sequence blockIdx.y.  Lane l owns latent columns 4l + 128 j (16-byte loads,
+// each warp access a contiguous 512-byte run).
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                const int32_t* __restrict__ seq_lens, int bs, int max_blocks, int B, int h,
                int d_c, int num_parts, void* __restrict__ o_lat, int o_dtype,
                float* __restrict__ lse_out) {
-  __shared__ float sw[kMaxSplits];
-  __shared__ float s_m, s_inv, s_lse;
   __shared__ int s_first, s_count;
-  const int s = blockIdx.x, b = blockIdx.y;
-  if (threadIdx.x < 32) {
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (warp == 0) {
     long long sb = 0;
     const long long T = warp_stream_scan(seq_lens, B, bs, max_blocks, b, -1, &sb, nullptr, nullptr);
     const int nb = seq_blocks(seq_lens, b, bs, max_blocks);
-    if (threadIdx.x == 0) {
+    if (lane == 0) {
       if (nb == 0) {
         s_first = 0;
         s_count = 0;
@@ -42,54 +44,33 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
     }
   }
   __syncthreads();
-  const int num_splits = s_count;
-  const int64_t lbase = (int64_t)s_first * h + s;   // lse of split j: lbase + j*h
+  const int s = blockIdx.x * kHeadsPerCta + warp;
+  if (s >= h) return;
+  const int first = s_first, count = s_count;
+  const float* lse_col = lse_part + (int64_t)first * h + s;   // split j at lse_col[j * h]
 
-  // maximum over splits
+  // maximum and weight sum over the splits (lanes stride over splits)
   float m = -INFINITY;
-  for (int j = threadIdx.x; j < num_splits; j += kThreads) m = fmaxf(m, lse_part[lbase + (int64_t)j * h]);
-  __shared__ float red[kThreads / 32];
+  for (int j = lane; j < count; j += 32) m = fmaxf(m, lse_col[(int64_t)j * h]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float mm = red[0];
-    for (int w = 1; w < kThreads / 32; ++w) mm = fmaxf(mm, red[w]);
-    s_m = mm;
-  }
-  __syncthreads();
-  m = s_m;
-  // weights
   float wsum = 0.f;
-  for (int j = threadIdx.x; j < num_splits; j += kThreads) {
-    float l = lse_part[lbase + (int64_t)j * h];
-    float w = (m == -INFINITY || l == -INFINITY) ? 0.f : expf(l - m);
-    sw[j] = w;
-    wsum += w;
+  for (int j = lane; j < count; j += 32) {
+    const float l = lse_col[(int64_t)j * h];
+    wsum += (m == -INFINITY || l == -INFINITY) ? 0.f : expf(l - m);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
-  __syncthreads();
-  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = wsum;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int w = 0; w < kThreads / 32; ++w) t += red[w];
-    s_inv = t > 0.f ? 1.f / t : 0.f;
-    s_lse = t > 0.f ? m + logf(t) : -INFINITY;
-  }
-  __syncthreads();
-  const float inv = s_inv;
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 
   const int64_t obase = ((int64_t)b * h + s) * d_c;
-  for (int c = threadIdx.x * 4; c < d_c; c += kThreads * 4) {
+  for (int c = 4 * lane; c < d_c; c += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < num_splits; ++j) {
-      float w = sw[j];
+    for (int j = 0; j < count; ++j) {
+      const float l = lse_col[(int64_t)j * h];
+      const float w = (m == -INFINITY || l == -INFINITY) ? 0.f : expf(l - m);
       if (w == 0.f) continue;
-      const float4 v = *reinterpret_cast<const float4*>(
-          o_part + (((int64_t)s_first + j) * h + s) * d_c + c);
+      const float4 v = *reinterpret_cast<const float4*>(o_part + (((int64_t)first + j) * h + s) * d_c + c);
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);
@@ -106,7 +87,8 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
       *reinterpret_cast<uint2*>(o) = pk;
     }
   }
-  if (lse_out && threadIdx.x == 0) lse_out[(int64_t)b * h + s] = s_lse;
+  if (lse_out && lane == 0)
+    lse_out[(int64_t)b * h + s] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
 }  // namespace
@@ -115,7 +97,7 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, const int
                            int block_size, int max_blocks, int B, int h, int d_c, int num_parts,
                            void* o_lat, int o_dtype, float* lse, cudaStream_t s) {
   if (num_parts > kMaxSplits) return cudaErrorInvalidValue;
-  dim3 grid(h, B);
+  dim3 grid(ceil_div(h, kHeadsPerCta), B);
   combine_kernel<<<grid, kThreads, 0, s>>>(o_part, lse_part, seq_lens, block_size, max_blocks, B,
                                            h, d_c, num_parts, o_lat, o_dtype, lse);
   return cudaGetLastError();

@@ -61,6 +61,24 @@ __host__ __device__ __forceinline__ int dtype_bytes(int dt) {
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------------------------
+// RoPE angles (iotdigitaltwinplm.com "MLA vs GQA vs MQA", the rope helper of
+// the listing: pair i of a d_r-vector at position pos is rotated by
+// pos * theta^(-2i/d_r))
+// ---------------------------------------------------------------------------
+
+// cos and sin of pos * inv_freq: the angle is formed and reduced modulo 2 pi in
+// float64 (positions reach 1e5 rad, where a float32 angle would be off by
+// ~1e-2), and the reduced angle (|r| <= pi) goes through float32 sincosf.
+__device__ __forceinline__ void rope_cos_sin(double pos, double inv_freq, float* c, float* s) {
+  const double two_pi = 6.283185307179586;
+  const double inv_two_pi = 0.15915494309189535;
+  const double ang = pos * inv_freq;
+  const double k = rint(ang * inv_two_pi);   // off by one at worst: |r| stays < pi + 1e-9
+  const float r = (float)fma(-k, two_pi, ang);
+  sincosf(r, s, c);
+}
+
+// ---------------------------------------------------------------------------
 // work partition of the decode (shared by the decode kernels and the combine)
 // ---------------------------------------------------------------------------
 //

@@ -54,8 +54,9 @@ namespace {
 using namespace tc;
 
 constexpr int kTok = 64;                    // tokens per tile (= cache block)
-constexpr int kStages = 4;
+constexpr int kMaxStages = 4;              // stage count of the bf16 variant (the larger)
 constexpr int kPrefetch = 6;                // tiles prefetched into L2 beyond the stages
+constexpr int kLandBytes = 64 * 256;        // FP8 variant: 64 tokens x 256 e4m3 codes
 constexpr int kGroups = 2;                  // softmax warpgroups (tile k goes to group k % kGroups)
 constexpr int kBoxBytes = 64 * 128;         // 64 rows x 64 bf16, 128-byte swizzle
 constexpr int kRopeBoxBytes = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
@@ -67,17 +68,28 @@ constexpr int kQRopeBytes = 128 * 64;       // query RoPE slice: 128 heads x 32 
 constexpr int kXChunks = 16;                // 16-byte chunks per row
 constexpr int kRecvBytes = 128 * kXChunks * 16;
 
-constexpr int kOffStages = 0;
-constexpr int kOffRecv = kOffStages + kStages * kStageBytes;
-constexpr int kOffQRope = kOffRecv + kGroups * kRecvBytes;  // 1024-aligned
-constexpr int kOffMpub = kOffQRope + kQRopeBytes;       // [2][128] float
-constexpr int kOffLstate = kOffMpub + 2 * 128 * 4;      // [2 seg][kGroups][128] float2
-constexpr int kOffBar = kOffLstate + 2 * kGroups * 128 * 8;
 constexpr int kNumBars = 32;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 64;
-constexpr int kSmemAlloc = kSmemBytes + 1024;  // alignment slack
-static_assert(kSmemAlloc <= 232448, "shared memory budget");
+
+// Layout of one variant: the bf16 cache (4 stages) or the FP8 latent cache (3
+// bf16 stages filled by converter warps from 2 FP8 landing buffers).
+template <bool kFp8>
+struct Cfg {
+  static constexpr int kStages = kFp8 ? 3 : kMaxStages;
+  static constexpr int kLand = kFp8 ? 2 : 0;
+  static constexpr int kThreads = 64 + 128 * kGroups + (kFp8 ? 64 : 0);
+  static constexpr int kOffStages = 0;
+  static constexpr int kOffLand = kOffStages + kStages * kStageBytes;
+  static constexpr int kOffRecv = kOffLand + kLand * kLandBytes;
+  static constexpr int kOffQRope = kOffRecv + kGroups * kRecvBytes;  // 1024-aligned
+  static constexpr int kOffMpub = kOffQRope + kQRopeBytes;       // [2][128] float
+  static constexpr int kOffLstate = kOffMpub + 2 * 128 * 4;      // [2 seg][kGroups][128] float2
+  static constexpr int kOffBar = kOffLstate + 2 * kGroups * 128 * 8;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 64;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;  // alignment slack
+  static_assert(kSmemAlloc <= 232448, "shared memory budget");
+  static_assert(kStages <= kMaxStages, "barrier array");
+};
 
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS = 256;
@@ -85,15 +97,16 @@ constexpr uint32_t kColQ = 320;   // latent query slice (bf16 pairs), 128 column
 constexpr uint32_t kColP = 448;   // [2] P (bf16 pairs, 32 columns each), A of the P.C MMA
 constexpr uint32_t kTmemCols = 512;
 
-constexpr int kThreads = 64 + 128 * kGroups;
 constexpr float kTau = 8.0f;  // lazy rescale threshold (log2 units): P stays <= 2^8
 constexpr float kLn2 = 0.69314718055994530942f;
 
 // barrier indices (derived from kStages so that the arrays never overlap)
 enum {
-  BAR_KV_FULL = 0,                      // [kStages] TMA -> MMA
-  BAR_KV_EMPTY = BAR_KV_FULL + kStages, // [kStages] MMA (commit after P.C) -> TMA
-  BAR_S_FULL = BAR_KV_EMPTY + kStages,  // [kGroups] MMA -> softmax group k % kGroups; one
+  BAR_KV_FULL = 0,                      // [kStages] TMA (+ FP8 converters) -> MMA
+  BAR_KV_EMPTY = BAR_KV_FULL + kMaxStages,  // [kStages] MMA (commit after P.C) -> TMA
+  BAR_LAND_FULL = BAR_KV_EMPTY + kMaxStages,  // [2] FP8: TMA -> converters
+  BAR_LAND_EMPTY = BAR_LAND_FULL + 2,   // [2] FP8: converters (2 warps) -> TMA
+  BAR_S_FULL = BAR_LAND_EMPTY + 2,      // [kGroups] MMA -> softmax group k % kGroups; one
                                         //     barrier per group so that a group's parity
                                         //     waits never alias another group's phases
   BAR_S_EMPTY = BAR_S_FULL + kGroups,   // softmax (4 warps) -> MMA
@@ -118,6 +131,7 @@ struct TcParams {
   float* o_part;                // [B + P - 1, h, 512]
   float* lse_part;              // [B + P - 1, h]
   int32_t* status;
+  const float* kv_scale;        // FP8 variant: per-block dequantisation scale [num_blocks]
   int max_blocks, B, h, num_parts, num_blocks;
   float scale_log2;
   long long wait_limit;
@@ -192,10 +206,16 @@ struct TileIter {
   }
 };
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                  const __grid_constant__ CUtensorMap tm_rope,
                  const __grid_constant__ CUtensorMap tm_q, const TcParams p) {
+  using C = Cfg<kFp8>;
+  constexpr int kStages = C::kStages, kThreads = C::kThreads;
+  constexpr int kOffStages = C::kOffStages, kOffLand = C::kOffLand, kOffRecv = C::kOffRecv;
+  constexpr int kOffQRope = C::kOffQRope, kOffMpub = C::kOffMpub, kOffLstate = C::kOffLstate;
+  constexpr int kOffBar = C::kOffBar, kOffMisc = C::kOffMisc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -212,8 +232,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(BAR_KV_FULL + s), 1);
+      mbar_init(bar(BAR_KV_FULL + s), kFp8 ? 3 : 1);   // FP8: + the two converter warps
       mbar_init(bar(BAR_KV_EMPTY + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(BAR_LAND_FULL + i), 1);
+      mbar_init(bar(BAR_LAND_EMPTY + i), 2);
     }
     mbar_init(bar(BAR_S_EMPTY), 4);
     for (int i = 0; i < kGroups; ++i) {
@@ -309,7 +333,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         for (; kp < kend && kp < ntiles; ++kp) {
           const int pb = p.block_table[(int64_t)pf.b * p.max_blocks + pf.blk];
           if (pb >= 0 && pb < p.num_blocks) {
-            for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tm_lat, (int)(rank * 4 + c) * 64, pb * kTok);
+            if constexpr (kFp8) {
+              tma_prefetch_2d(&tm_lat, (int)rank * 256, pb * kTok);
+            } else {
+              for (int c = 0; c < 4; ++c)
+                tma_prefetch_2d(&tm_lat, (int)(rank * 4 + c) * 64, pb * kTok);
+            }
             tma_prefetch_2d(&tm_rope, (int)rank * 32, pb * kTok);
           }
           if (kp + 1 < ntiles) pf.next();
@@ -334,11 +363,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         MLA_TR(k, 0);
         const uint32_t dst = sbase + kOffStages + st * kStageBytes;
         const uint32_t fb = bar(BAR_KV_FULL + st);
-        mbar_arrive_expect_tx(fb, tx);
         const int y = pb * kTok;
-        for (int c = 0; c < 4; ++c)
-          tma_load_2d(dst + c * kBoxBytes, &tm_lat, (int)(rank * 4 + c) * 64, y, fb);
-        tma_load_2d(dst + 4 * kBoxBytes, &tm_rope, (int)rank * 32, y, fb);
+        if constexpr (kFp8) {
+          // e4m3 codes of this CTA's 256 latent columns -> landing buffer j; the
+          // converter warps write the bf16 latent boxes of stage st from it
+          const int j = k % 2;
+          if (k >= 2 && !mbar_wait_or_abort(bar(BAR_LAND_EMPTY + j), ((k / 2) - 1) & 1, lim,
+                                            abort_flag, &timed_out)) {
+            fail();
+            break;
+          }
+          reinterpret_cast<volatile int*>(smem + kOffMisc + 32)[j] = pb;
+          mbar_arrive_expect_tx(fb, kRopeBoxBytes);
+          tma_load_2d(dst + 4 * kBoxBytes, &tm_rope, (int)rank * 32, y, fb);
+          mbar_arrive_expect_tx(bar(BAR_LAND_FULL + j), kLandBytes);
+          tma_load_2d(sbase + kOffLand + j * kLandBytes, &tm_lat, (int)rank * 256, y,
+                      bar(BAR_LAND_FULL + j));
+        } else {
+          mbar_arrive_expect_tx(fb, tx);
+          for (int c = 0; c < 4; ++c)
+            tma_load_2d(dst + c * kBoxBytes, &tm_lat, (int)(rank * 4 + c) * 64, y, fb);
+          tma_load_2d(dst + 4 * kBoxBytes, &tm_rope, (int)rank * 32, y, fb);
+        }
         if (k + 1 < ntiles) it.next();
       }
       // every issued load must land before the CTA may exit
@@ -348,6 +394,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (n > 0) {
           int never = 0;
           mbar_wait_or_abort(bar(BAR_KV_FULL + st), (n - 1) & 1, lim, &never, &dummy);
+        }
+      }
+      if constexpr (kFp8) {
+        for (int j = 0; j < 2; ++j) {
+          const int n = (k - j + 1) / 2;  // loads issued into landing buffer j
+          if (n > 0) {
+            int never = 0;
+            mbar_wait_or_abort(bar(BAR_LAND_FULL + j), (n - 1) & 1, lim, &never, &dummy);
+          }
         }
       }
     }
@@ -493,7 +548,52 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       mbar_wait_or_abort(bar(BAR_DRAIN), 0, lim, &never, &dummy);
     }
     __syncwarp();
-  } else if (b_first >= 0 && ntiles > 0 && warp >= 2) {
+  } else if (kFp8 && b_first >= 0 && ntiles > 0 && warp >= 2 + 4 * kGroups) {
+    // ------------------------------------------------------------ FP8 converters
+    // Landing buffer j holds the e4m3 codes of 64 tokens x this CTA's 256 latent
+    // columns (row-major, 256 B per token).  Each code becomes
+    // bf16(e4m3 value x block scale) in the 128-byte-swizzled bf16 boxes of
+    // stage st, where the MMAs read it (kexue.fm / iotdigitaltwinplm: the
+    // latent is stored in FP8; one float32 scale per 64-token block).
+    const int ct = threadIdx.x - 32 * (2 + 4 * kGroups);  // 0..63
+    const volatile int* land_pb = reinterpret_cast<const volatile int*>(smem + kOffMisc + 32);
+    bool ok = true;
+    for (int k = 0; k < ntiles; ++k) {
+      const int j = k % 2, st = k % kStages;
+      if (!warp_wait(bar(BAR_LAND_FULL + j), (k / 2) & 1)) { ok = false; break; }
+      const float sc = p.kv_scale[land_pb[j]];
+      const uint8_t* src = smem + kOffLand + j * kLandBytes;
+      uint8_t* dst = smem + kOffStages + st * kStageBytes;
+      for (int i = ct; i < 64 * 16; i += 64) {
+        const int r = i >> 4, q = i & 15;           // token row, 16-code group
+        const uint4 v = *reinterpret_cast<const uint4*>(src + r * 256 + q * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>((w[e] >> (16 * hh)) & 0xFFFFu), __NV_E4M3);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            o[2 * e + hh] = pack_bf16x2(f.x * sc, f.y * sc);
+          }
+        }
+        // codes 16q .. 16q+15 = latent columns of box q / 4, chunks 2 (q % 4) and +1
+        const int box = q >> 2, c0 = 2 * (q & 3);
+        uint8_t* rowp = dst + box * kBoxBytes + r * 128;
+        *reinterpret_cast<uint4*>(rowp + ((c0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(BAR_LAND_EMPTY + j));
+        mbar_arrive(bar(BAR_KV_FULL + st));
+      }
+    }
+    if (!ok) fail();
+  } else if (b_first >= 0 && ntiles > 0 && warp >= 2 && warp < 2 + 4 * kGroups) {
     // ------------------------------------------------------------ softmax groups
     const int g = (warp - 2) >> 2;            // group: tiles k with k % kGroups == g
     const int sub = warp & 3;                 // TMEM sub-partition of this warp
@@ -838,28 +938,60 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 bool tc_device() { return device_major() >= 10 && get_encode_fn() != nullptr; }
 
 bool decode_tc_supported(int q_dtype, const mla_kv_cache& kv, int h) {
-  return q_dtype == MLA_BF16 && kv.latent_dtype == MLA_BF16 && kv.rope_dtype == MLA_BF16 &&
-         kv.d_c == 512 && kv.d_r == 64 && kv.block_size == kTok && h >= 1 && h <= 128 &&
-         tc_device();
+  const bool lat_ok = kv.latent_dtype == MLA_BF16 || (kv.latent_dtype == MLA_FP8E4M3 && kv.scale);
+  return q_dtype == MLA_BF16 && lat_ok && kv.rope_dtype == MLA_BF16 && kv.d_c == 512 &&
+         kv.d_r == 64 && kv.block_size == kTok && h >= 1 && h <= 128 && tc_device();
 }
+
+namespace {
+
+// e4m3 latent view [rows, 512] (bytes), boxes of 256 codes x 64 rows, no swizzle.
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_pitch_bytes) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {512, rows};
+  cuuint64_t strides[1] = {row_pitch_bytes};
+  cuuint32_t box[2] = {256, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool kFp8>
+cudaError_t launch_variant(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope,
+                           const CUtensorMap& tm_q, const TcParams& prm, int num_parts,
+                           cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<kFp8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<kFp8>::kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(2 * num_parts);
+  decode_tc_kernel<kFp8><<<grid, Cfg<kFp8>::kThreads, Cfg<kFp8>::kSmemAlloc, s>>>(tm_lat, tm_rope,
+                                                                                 tm_q, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                              int B, int h, int num_parts, float scale, float* o_part,
                              float* lse_part, int32_t* status, cudaStream_t s) {
+  const bool fp8 = kv.latent_dtype == MLA_FP8E4M3;
   CUtensorMap tm_lat, tm_rope, tm_q;
   const uint64_t rows = (uint64_t)kv.num_blocks * kv.block_size;
-  if (!make_tmap(&tm_lat, kv.latent, 512, rows, (uint64_t)kv.latent_stride * 2, 64, 64) ||
-      !make_tmap(&tm_rope, kv.rope, 64, rows, (uint64_t)kv.rope_stride * 2, 32, 64) ||
+  const bool lat_ok =
+      fp8 ? make_tmap_u8(&tm_lat, kv.latent, rows, (uint64_t)kv.latent_stride)
+          : make_tmap(&tm_lat, kv.latent, 512, rows, (uint64_t)kv.latent_stride * 2, 64, 64);
+  if (!lat_ok || !make_tmap(&tm_rope, kv.rope, 64, rows, (uint64_t)kv.rope_stride * 2, 32, 64) ||
       !make_tmap(&tm_q, q_cat, 576, (uint64_t)B * h, 576 * 2, 32, 128))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   TcParams prm;
   prm.q_cat = static_cast<const uint16_t*>(q_cat);
   prm.block_table = block_table;
@@ -867,6 +999,7 @@ cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
   prm.o_part = o_part;
   prm.lse_part = lse_part;
   prm.status = status;
+  prm.kv_scale = kv.scale;
   prm.max_blocks = max_blocks;
   prm.B = B;
   prm.h = h;
@@ -874,9 +1007,8 @@ cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
   prm.num_blocks = kv.num_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.wait_limit = 4000000000LL;  // about 2 s of SM clock
-  dim3 grid(2 * num_parts);
-  decode_tc_kernel<<<grid, kThreads, kSmemAlloc, s>>>(tm_lat, tm_rope, tm_q, prm);
-  return cudaGetLastError();
+  return fp8 ? launch_variant<true>(tm_lat, tm_rope, tm_q, prm, num_parts, s)
+             : launch_variant<false>(tm_lat, tm_rope, tm_q, prm, num_parts, s);
 }
 
 }  // namespace mla

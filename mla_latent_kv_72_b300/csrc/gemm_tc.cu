@@ -146,14 +146,15 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 
   // rotary query part (absorb, m tile 0): independent of the MMA
   if (p.q_rope != nullptr && mt == 0) {
+    __shared__ double inv_freq[32];
+    if (threadIdx.x < 32) inv_freq[threadIdx.x] = pow(p.theta, -2.0 * (double)threadIdx.x / 64.0);
+    __syncthreads();
     const int nb = min(p.n_tile, p.B - b0);
     uint16_t* q_cat = static_cast<uint16_t*>(p.out);
     for (int i = threadIdx.x; i < nb * 32; i += kGThreads) {
       const int bb = b0 + i / 32, pr = i % 32;
-      const double inv = pow(p.theta, -2.0 * (double)pr / 64.0);
-      double sd, cd;
-      sincos((double)p.q_pos[bb] * inv, &sd, &cd);
-      const float cs = (float)cd, sn = (float)sd;
+      float cs, sn;
+      rope_cos_sin((double)p.q_pos[bb], inv_freq[pr], &cs, &sn);
       const int64_t ib = ((int64_t)bb * p.h + s) * 64;
       const float x0 = bf16_to_f32(p.q_rope[ib + 2 * pr]);
       const float x1 = bf16_to_f32(p.q_rope[ib + 2 * pr + 1]);
@@ -226,8 +227,9 @@ bool encode(CUtensorMap* m, int rank, const void* base, const cuuint64_t* dims,
   return r == CUDA_SUCCESS;
 }
 
-int n_tile_for(int B) {
-  int n = B < kMaxN ? B : kMaxN;
+// batch rows per CTA: at most cap (a multiple of 16), rounded up to 16
+int n_tile_for(int B, int cap = kMaxN) {
+  int n = B < cap ? B : cap;
   return (n + 15) / 16 * 16;
 }
 
@@ -286,7 +288,8 @@ cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, i
   cuuint64_t adims[2] = {512, (cuuint64_t)h * 128};
   cuuint64_t astr[1] = {512 * 2};
   cuuint32_t abox[2] = {64, 128};
-  const int nt = n_tile_for(B);
+  // 32 batch rows per CTA: more CTAs stream W_UV (from L2 after the first) in parallel
+  const int nt = n_tile_for(B, 32);
   cuuint64_t xdims[3] = {512, (cuuint64_t)h, (cuuint64_t)B};
   cuuint64_t xstr[2] = {512 * 2, (cuuint64_t)h * 512 * 2};
   cuuint32_t xbox[3] = {64, 1, (cuuint32_t)nt};
