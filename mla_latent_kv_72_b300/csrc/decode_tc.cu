@@ -57,7 +57,14 @@ constexpr int kTok = 64;                    // tokens per tile (= cache block)
 constexpr int kMaxStages = 4;              // stage count of the bf16 variant (the larger)
 constexpr int kPrefetch = 6;                // tiles prefetched into L2 beyond the stages
 constexpr int kLandBytes = 64 * 256;        // FP8 variant: 64 tokens x 256 e4m3 codes
-constexpr int kGroups = 2;                  // softmax warpgroups (tile k goes to group k % kGroups)
+constexpr int kGroups = 2;                  // softmax groups (tile k goes to group k % kGroups)
+// warps per TMEM lane quarter in a softmax group: with 2, a row's 64 scores are
+// split between two warps (columns [32 hf, 32 hf + 32)), which halves each
+// thread's share of the per-tile chain; the row maximum then meets in shared memory
+constexpr int kHalves = 2;
+constexpr int kCols = 64 / kHalves;         // score columns per softmax thread
+constexpr int kGroupWarps = 4 * kHalves;
+constexpr int kSoftWarps = kGroups * kGroupWarps;
 constexpr int kBoxBytes = 64 * 128;         // 64 rows x 64 bf16, 128-byte swizzle
 constexpr int kRopeBoxBytes = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
 constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // 4 latent boxes + half the RoPE dims
@@ -76,14 +83,18 @@ template <bool kFp8>
 struct Cfg {
   static constexpr int kStages = kFp8 ? 3 : kMaxStages;
   static constexpr int kLand = kFp8 ? 2 : 0;
-  static constexpr int kThreads = 64 + 128 * kGroups + (kFp8 ? 64 : 0);
+  // bf16: one more warp issues the P.C MMAs (warp 2 + kSoftWarps); FP8: two converter warps
+  static constexpr bool kSplitMma = !kFp8;
+  static constexpr int kThreads = 64 + 32 * kSoftWarps + (kFp8 ? 64 : 32);
   static constexpr int kOffStages = 0;
   static constexpr int kOffLand = kOffStages + kStages * kStageBytes;
   static constexpr int kOffRecv = kOffLand + kLand * kLandBytes;
   static constexpr int kOffQRope = kOffRecv + kGroups * kRecvBytes;  // 1024-aligned
   static constexpr int kOffMpub = kOffQRope + kQRopeBytes;       // [2][128] float
-  static constexpr int kOffLstate = kOffMpub + 2 * 128 * 4;      // [2 seg][kGroups][128] float2
-  static constexpr int kOffBar = kOffLstate + 2 * kGroups * 128 * 8;
+  static constexpr int kOffLm = kOffMpub + 2 * 128 * 4;          // [2 seg][kGroups][128] float: m
+  static constexpr int kOffLs = kOffLm + 2 * kGroups * 128 * 4;  // [2 seg][kGroups][kHalves][128] l
+  static constexpr int kOffHmax = kOffLs + 2 * kGroups * kHalves * 128 * 4;  // [kGroups][kHalves][128]
+  static constexpr int kOffBar = kOffHmax + (kHalves > 1 ? kGroups * kHalves * 128 * 4 : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 64;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // alignment slack
@@ -109,18 +120,20 @@ enum {
   BAR_S_FULL = BAR_LAND_EMPTY + 2,      // [kGroups] MMA -> softmax group k % kGroups; one
                                         //     barrier per group so that a group's parity
                                         //     waits never alias another group's phases
-  BAR_S_EMPTY = BAR_S_FULL + kGroups,   // softmax (4 warps) -> MMA
-  BAR_P_FULL = BAR_S_EMPTY + 1,         // [2] softmax (4 warps) -> MMA, by P buffer k & 1
+  BAR_S_EMPTY = BAR_S_FULL + kGroups,   // softmax (a group's warps) -> MMA
+  BAR_P_FULL = BAR_S_EMPTY + 1,         // [2] softmax (a group's warps) -> MMA, by P buffer k & 1
   BAR_O_DONE = BAR_P_FULL + 2,          // [4] MMA -> softmax, by k & 3 (P buffer free, O final);
                                         //     four so that no waiter can be two phases off
-  BAR_PEER_FREE = BAR_O_DONE + 4,       // [kGroups] peer's 4 warps have read what we sent
-  BAR_MREADY = BAR_PEER_FREE + kGroups, // [2] running maximum of tile k published, by k & 1
+  BAR_PEER_FREE = BAR_O_DONE + 4,       // [kGroups] peer group's warps have read what we sent
+  BAR_MREADY = BAR_PEER_FREE + kGroups, // [2] running maximum of tile k published and the
+                                        //     previous one read by every warp of the group
   BAR_Q_FREE = BAR_MREADY + 2,          // MMA: last score MMA of a segment done
-  BAR_Q_READY = BAR_Q_FREE + 1,         // softmax (8 warps) + TMA of the RoPE query slice
-  BAR_O_FREE = BAR_Q_READY + 1,         // softmax (8 warps): O of a segment read out
-  BAR_SEG = BAR_O_FREE + 1,             // softmax (8 warps): end-of-segment rendezvous
+  BAR_Q_READY = BAR_Q_FREE + 1,         // softmax (all warps) + TMA of the RoPE query slice
+  BAR_O_FREE = BAR_Q_READY + 1,         // softmax (all warps): O of a segment read out
+  BAR_SEG = BAR_O_FREE + 1,             // softmax (all warps): end-of-segment rendezvous
   BAR_DRAIN = BAR_SEG + 1,
-  BAR_COUNT = BAR_DRAIN + 1,
+  BAR_DRAIN_O = BAR_DRAIN + 1,          // bf16 variant: the P.C issuer's own drain
+  BAR_COUNT = BAR_DRAIN_O + 1,
 };
 static_assert(BAR_COUNT <= kNumBars, "barrier array");
 
@@ -214,7 +227,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
   using C = Cfg<kFp8>;
   constexpr int kStages = C::kStages, kThreads = C::kThreads;
   constexpr int kOffStages = C::kOffStages, kOffLand = C::kOffLand, kOffRecv = C::kOffRecv;
-  constexpr int kOffQRope = C::kOffQRope, kOffMpub = C::kOffMpub, kOffLstate = C::kOffLstate;
+  constexpr int kOffQRope = C::kOffQRope, kOffMpub = C::kOffMpub;
   constexpr int kOffBar = C::kOffBar, kOffMisc = C::kOffMisc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -239,21 +252,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       mbar_init(bar(BAR_LAND_FULL + i), 1);
       mbar_init(bar(BAR_LAND_EMPTY + i), 2);
     }
-    mbar_init(bar(BAR_S_EMPTY), 4);
+    mbar_init(bar(BAR_S_EMPTY), kGroupWarps);
     for (int i = 0; i < kGroups; ++i) {
       mbar_init(bar(BAR_S_FULL + i), 1);
-      mbar_init(bar(BAR_PEER_FREE + i), 4);
+      mbar_init(bar(BAR_PEER_FREE + i), kGroupWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(BAR_P_FULL + i), 4);
-      mbar_init(bar(BAR_MREADY + i), 4);
+      mbar_init(bar(BAR_P_FULL + i), kGroupWarps);
+      mbar_init(bar(BAR_MREADY + i), kGroupWarps);
     }
     for (int i = 0; i < 4; ++i) mbar_init(bar(BAR_O_DONE + i), 1);
     mbar_init(bar(BAR_Q_FREE), 1);
-    mbar_init(bar(BAR_Q_READY), 4 * kGroups + 1);
-    mbar_init(bar(BAR_O_FREE), 4 * kGroups);
-    mbar_init(bar(BAR_SEG), 4 * kGroups);
+    mbar_init(bar(BAR_Q_READY), kSoftWarps + 1);
+    mbar_init(bar(BAR_O_FREE), kSoftWarps);
+    mbar_init(bar(BAR_SEG), kSoftWarps);
     mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_DRAIN_O), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -341,6 +355,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             }
             tma_prefetch_2d(&tm_rope, (int)rank * 32, pb * kTok);
           }
+          if (pf.blk == 0 && kp > 0) {
+            // a later segment starts here: its query rows (this CTA's latent
+            // slice and RoPE dims) go to L2 ahead of the segment's query load
+            for (int j = 0; j < 8; ++j) tma_prefetch_2d(&tm_q, 256 * (int)rank + 32 * j, pf.b * p.h);
+            tma_prefetch_2d(&tm_q, 512 + 32 * (int)rank, pf.b * p.h);
+          }
           if (kp + 1 < ntiles) pf.next();
         }
       };
@@ -406,6 +426,109 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         }
       }
     }
+  } else if (C::kSplitMma && b_first >= 0 && ntiles > 0 && warp == 1) {
+    // ------------------------------------------------------------ score MMA issuer (bf16)
+    // S(k) needs its stage (KV_FULL), the previous tile's scores loaded out
+    // (S_EMPTY) and, at a segment start, the segment's query; blocking waits,
+    // so the warp sleeps until its inputs are there.  The P.C MMAs come from
+    // their own warp: a P.C never waits behind a score MMA being issued.
+    const uint32_t idS = idesc_bf16_f32(128, 64, false, false);
+    TileIter its;
+    its.init(p.seq_lens, p.max_blocks, b_first, blk_first);
+    int seg_s = 0;
+    bool ok = true;
+    for (int ks = 0; ks < ntiles; ++ks) {
+      const int st = ks % kStages;
+      const bool first = (ks == 0) || (its.blk == 0);
+      const bool last = (ks == ntiles - 1) || (its.blk == its.nb - 1);
+      if (first && !warp_wait(bar(BAR_Q_READY), seg_s & 1)) { ok = false; break; }
+      if (!warp_wait(bar(BAR_KV_FULL + st), (ks / kStages) & 1)) { ok = false; break; }
+      if (ks > 0 && !warp_wait(bar(BAR_S_EMPTY), (ks - 1) & 1)) { ok = false; break; }
+      const int n_valid = its.valid();
+      if (n_valid < kTok) {
+        // slots past the sequence end: zero them so that P = 0 meets finite values
+        uint8_t* sp = smem + kOffStages + st * kStageBytes;
+        const int nrow = kTok - n_valid;
+        for (int e = lane; e < 4 * nrow * 8; e += 32) {
+          const int box = e / (nrow * 8), rr = (e / 8) % nrow, ch = e % 8;
+          *reinterpret_cast<uint4*>(sp + box * kBoxBytes + (n_valid + rr) * 128 + ch * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        for (int e = lane; e < nrow * 4; e += 32)
+          *reinterpret_cast<uint4*>(sp + 4 * kBoxBytes + (n_valid + e / 4) * 64 + (e % 4) * 16) =
+              make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      tc_fence_after();
+      if (lane == 0) {
+        MLA_TR(ks, 1);
+        const uint32_t stage = sbase + kOffStages + st * kStageBytes;
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint64_t bd = smem_desc(stage + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024,
+                                        kSwizzle128B);
+          mma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bd, idS, kk > 0 ? 1u : 0u);
+        }
+        for (int kk = 0; kk < 2; ++kk) {
+          const uint64_t ad = smem_desc(sbase + kOffQRope + kk * 32, 16, 512, kSwizzle64B);
+          const uint64_t bd = smem_desc(stage + 4 * kBoxBytes + kk * 32, 16, 512, kSwizzle64B);
+          mma_ss(tmem + kColS, ad, bd, idS, 1u);
+        }
+        mma_commit(bar(BAR_S_FULL + (ks % kGroups)));
+        if (last) mma_commit(bar(BAR_Q_FREE));
+      }
+      __syncwarp();
+      if (last) ++seg_s;
+      if (ks + 1 < ntiles) its.next();
+    }
+    if (!ok) fail();
+    if (lane == 0) {
+      mma_commit(bar(BAR_DRAIN));
+      int never = 0;
+      bool dummy = false;
+      mbar_wait_or_abort(bar(BAR_DRAIN), 0, lim, &never, &dummy);
+    }
+    __syncwarp();
+  } else if (C::kSplitMma && b_first >= 0 && ntiles > 0 && warp == 2 + kSoftWarps) {
+    // ------------------------------------------------------------ P.C MMA issuer (bf16)
+    // O(k) += P(k) C(k) once P(k) is in TMEM (S(k) is complete by then, so the
+    // commit after O(k) also covers the last reader of the stage); the first
+    // tile of a segment overwrites O after the previous segment's epilogue.
+    const uint32_t idO = idesc_bf16_f32(128, 256, false, true);
+    TileIter ito;
+    ito.init(p.seq_lens, p.max_blocks, b_first, blk_first);
+    int seg_o = 0;
+    bool ok = true;
+    for (int ko = 0; ko < ntiles; ++ko) {
+      const bool first = (ko == 0) || (ito.blk == 0);
+      const bool last = (ko == ntiles - 1) || (ito.blk == ito.nb - 1);
+      if (first && seg_o > 0 && !warp_wait(bar(BAR_O_FREE), (seg_o - 1) & 1)) { ok = false; break; }
+      if (!warp_wait(bar(BAR_P_FULL + (ko & 1)), (ko >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) {
+        MLA_TR(ko, 2);
+        const uint32_t stage = sbase + kOffStages + (ko % kStages) * kStageBytes;
+        const uint32_t pcol = kColP + 32 * (ko & 1);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint64_t bd = smem_desc(stage + c * 2048, kBoxBytes, 1024, kSwizzle128B);
+          mma_ts(tmem + kColO, tmem + pcol + 8 * c, bd, idO, (first && c == 0) ? 0u : 1u);
+        }
+        mma_commit(bar(BAR_O_DONE + (ko & 3)));
+        mma_commit(bar(BAR_KV_EMPTY + (ko % kStages)));
+      }
+      __syncwarp();
+      if (last) ++seg_o;
+      if (ko + 1 < ntiles) ito.next();
+    }
+    if (!ok) fail();
+    if (lane == 0) {
+      mma_commit(bar(BAR_DRAIN_O));
+      int never = 0;
+      bool dummy = false;
+      mbar_wait_or_abort(bar(BAR_DRAIN_O), 0, lim, &never, &dummy);
+    }
+    __syncwarp();
   } else if (b_first >= 0 && ntiles > 0 && warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Event-driven: whichever of the next score MMA S(ks) and the next P.C MMA
@@ -548,14 +671,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       mbar_wait_or_abort(bar(BAR_DRAIN), 0, lim, &never, &dummy);
     }
     __syncwarp();
-  } else if (kFp8 && b_first >= 0 && ntiles > 0 && warp >= 2 + 4 * kGroups) {
+  } else if (kFp8 && b_first >= 0 && ntiles > 0 && warp >= 2 + kSoftWarps) {
     // ------------------------------------------------------------ FP8 converters
     // Landing buffer j holds the e4m3 codes of 64 tokens x this CTA's 256 latent
     // columns (row-major, 256 B per token).  Each code becomes
     // bf16(e4m3 value x block scale) in the 128-byte-swizzled bf16 boxes of
     // stage st, where the MMAs read it (kexue.fm / iotdigitaltwinplm: the
     // latent is stored in FP8; one float32 scale per 64-token block).
-    const int ct = threadIdx.x - 32 * (2 + 4 * kGroups);  // 0..63
+    const int ct = threadIdx.x - 32 * (2 + kSoftWarps);  // 0..63
     const volatile int* land_pb = reinterpret_cast<const volatile int*>(smem + kOffMisc + 32);
     bool ok = true;
     for (int k = 0; k < ntiles; ++k) {
@@ -593,28 +716,42 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       }
     }
     if (!ok) fail();
-  } else if (b_first >= 0 && ntiles > 0 && warp >= 2 && warp < 2 + 4 * kGroups) {
+  } else if (b_first >= 0 && ntiles > 0 && warp >= 2 && warp < 2 + kSoftWarps) {
     // ------------------------------------------------------------ softmax groups
-    const int g = (warp - 2) >> 2;            // group: tiles k with k % kGroups == g
+    const int wg = (warp - 2) % kGroupWarps;  // warp within the group
+    const int g = (warp - 2) / kGroupWarps;   // group: tiles k with k % kGroups == g
+    const int hf = wg >> 2;                   // column half: score columns [kCols hf, +kCols)
     const int sub = warp & 3;                 // TMEM sub-partition of this warp
     const int row = sub * 32 + lane;          // head
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
     const bool live = row < p.h;
-    const bool group_lead = (warp == 2 + 4 * g) && lane == 0;
+    const bool group_lead = wg == 0 && lane == 0;
     float* mpub = reinterpret_cast<float*>(smem + kOffMpub);
-    float2* lstate = reinterpret_cast<float2*>(smem + kOffLstate);
+    float* lm = reinterpret_cast<float*>(smem + C::kOffLm);
+    float* lsum = reinterpret_cast<float*>(smem + C::kOffLs);
+    float* hmax = reinterpret_cast<float*>(smem + C::kOffHmax);
+    // the two warps of this group that share TMEM lane quarter sub meet on
+    // named barrier 1 + 4 g + sub (64 threads)
+    auto pair_sync = [&]() {
+      if constexpr (kHalves > 1)
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + 4 * g + sub) : "memory");
+    };
     // exchange buffers: chunk c (16 B) of row sub * 32 + lane at
     // (sub * kXChunks + c) * 512 + lane * 16, so that a warp's stores and loads
-    // are contiguous 512-byte runs
-    const uint32_t xoff = (uint32_t)(sub * kXChunks * 512 + lane * 16);
+    // are contiguous 512-byte runs; this thread owns chunks [kCols/4 hf, +kCols/4)
+    constexpr int kMyChunks = kCols / 4;
+    const uint32_t xoff = (uint32_t)((sub * kXChunks + kMyChunks * hf) * 512 + lane * 16);
     const uint8_t* my_recv = smem + kOffRecv + g * kRecvBytes + xoff;
     const uint32_t my_recv_u32 = sbase + kOffRecv + g * kRecvBytes + xoff;
     const uint32_t peer_recv = mapa(sbase + kOffRecv + g * kRecvBytes + xoff, peer);
     const uint32_t peer_free = mapa(bar(BAR_PEER_FREE + g), peer);
 
-    // query slice of sequence b -> TMEM (A operand).  CTA 0 holds dims
-    // [0, 256) ++ [512, 576), CTA 1 dims [256, 512); 16-column chunks (32
-    // dims) are split between the two groups.
+    // query slice of sequence b -> TMEM (A operand).  CTA r holds latent dims
+    // [256 r, 256 r + 256) (TMEM) and RoPE dims [512 + 32 r, +32) (shared
+    // memory); the eight 16-column chunks (32 dims each) are split between
+    // the softmax threads of a row.
+    constexpr int kQChunks = 8 / (kGroups * kHalves);
+    static_assert(kQChunks * kGroups * kHalves == 8, "query chunks per thread");
     auto load_q = [&](int b) {
       if (group_lead && g == 0) {
         // RoPE dims [512 + 32 rank, +32) of the 128 query rows of sequence b
@@ -622,19 +759,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         tma_load_2d(sbase + kOffQRope, &tm_q, 512 + 32 * (int)rank, b * p.h, bar(BAR_Q_READY));
       }
       const uint4* q = reinterpret_cast<const uint4*>(p.q_cat + ((int64_t)b * p.h + (live ? row : 0)) * 576);
-      for (int c = (8 * g) / kGroups; c < (8 * (g + 1)) / kGroups; ++c) {
-        const int dim0 = 256 * (int)rank + 32 * c;
-        uint32_t w[16];
+      const int qc0 = (g * kHalves + hf) * kQChunks;
+      // all loads first (one memory round trip), then the TMEM stores
+      uint32_t w[kQChunks][16];
+#pragma unroll
+      for (int cc = 0; cc < kQChunks; ++cc) {
+        const int dim0 = 256 * (int)rank + 32 * (qc0 + cc);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint4 v = live ? q[dim0 / 8 + u] : make_uint4(0, 0, 0, 0);
-          w[4 * u + 0] = v.x;
-          w[4 * u + 1] = v.y;
-          w[4 * u + 2] = v.z;
-          w[4 * u + 3] = v.w;
+          const uint4 v = live ? __ldg(q + dim0 / 8 + u) : make_uint4(0, 0, 0, 0);
+          w[cc][4 * u + 0] = v.x;
+          w[cc][4 * u + 1] = v.y;
+          w[cc][4 * u + 2] = v.z;
+          w[cc][4 * u + 3] = v.w;
         }
-        tmem_st16(tl + kColQ + 16 * c, w);
       }
+#pragma unroll
+      for (int cc = 0; cc < kQChunks; ++cc) tmem_st16(tl + kColQ + 16 * (qc0 + cc), w[cc]);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -643,7 +784,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
     TileIter it;
     it.init(p.seq_lens, p.max_blocks, b_first, blk_first);
-    float m_g = -INFINITY, l_g = 0.f;   // running max / sum of this group's tiles
+    float m_g = -INFINITY, l_g = 0.f;   // running max / sum (this thread's columns) of this group's tiles
     int seg = 0;
     bool ok = true;
     load_q(it.b);
@@ -655,15 +796,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       if (k % kGroups == g) {
         const int u = k / kGroups;  // use index of this group's exchange buffers
         const int n_valid = it.valid();
-        // ---- partial scores of this CTA
+        // ---- partial scores of this CTA, this thread's columns
         if (!warp_wait(bar(BAR_S_FULL + g), u & 1)) { ok = false; break; }
         if (group_lead) MLA_TR(k, 3);
         tc_fence_after();
-        uint32_t r[64];
-        tmem_ld16(tl + kColS + 0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-        tmem_ld16(tl + kColS + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
-        tmem_ld16(tl + kColS + 32, *reinterpret_cast<uint32_t(*)[16]>(&r[32]));
-        tmem_ld16(tl + kColS + 48, *reinterpret_cast<uint32_t(*)[16]>(&r[48]));
+        uint32_t r[kCols];
+#pragma unroll
+        for (int c = 0; c < kCols / 16; ++c)
+          tmem_ld16(tl + kColS + kCols * hf + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * c]));
         tmem_wait_ld();
         if (group_lead) MLA_TR(k, 9);
         tc_fence_before();
@@ -679,15 +819,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         // of every value sent carries the use tag (1..255)
         const uint32_t tag = (uint32_t)(u % 255) + 1u;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) r[i] &= 0xFFFFFF00u;
+        for (int i = 0; i < kCols; ++i) r[i] &= 0xFFFFFF00u;
 #pragma unroll
-        for (int c = 0; c < kXChunks; ++c)
+        for (int c = 0; c < kMyChunks; ++c)
           st_cluster_v4(peer_recv + c * 512, __uint_as_float(r[4 * c] | tag),
                         __uint_as_float(r[4 * c + 1] | tag), __uint_as_float(r[4 * c + 2] | tag),
                         __uint_as_float(r[4 * c + 3] | tag));
         if (group_lead) MLA_TR(k, 11);
         if (group_lead) MLA_TR(k, 4);
-        // poll the local buffer until all 64 values of this row carry the tag
+        // poll the local buffer until all of this thread's values carry the tag
         // (each 4-byte value is written atomically, so a tagged value is whole)
         {
           const long long t0 = clock64();
@@ -695,7 +835,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           while (true) {
             bool mine = true;
 #pragma unroll
-            for (int c = 0; c < kXChunks; ++c) {
+            for (int c = 0; c < kMyChunks; ++c) {
               uint32_t v0, v1, v2, v3;
               asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
@@ -718,7 +858,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         // full score (log2 domain) in place: r <- (own partial + peer's) * scale
         float mt = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kXChunks; ++c) {
+        for (int c = 0; c < kMyChunks; ++c) {
           const uint4 v = *reinterpret_cast<const uint4*>(my_recv + c * 512);
           const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -734,11 +874,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (lane == 0) mbar_arrive_remote_relaxed(peer_free);
         if (n_valid < kTok) {  // ragged last block: slots past the end get -inf
 #pragma unroll
-          for (int kk = 0; kk < 64; ++kk)
-            if (kk >= n_valid) r[kk] = __float_as_uint(-INFINITY);
+          for (int kk = 0; kk < kCols; ++kk)
+            if (kCols * hf + kk >= n_valid) r[kk] = __float_as_uint(-INFINITY);
         }
 #pragma unroll
-        for (int kk = 0; kk < 64; ++kk) mt = fmaxf(mt, __uint_as_float(r[kk]));
+        for (int kk = 0; kk < kCols; ++kk) mt = fmaxf(mt, __uint_as_float(r[kk]));
+        if constexpr (kHalves > 1) {
+          // row maximum over both halves: the first meeting makes sure that the
+          // partner has read what this thread wrote for the group's previous tile
+          pair_sync();
+          hmax[(g * kHalves + hf) * 128 + row] = mt;
+          pair_sync();
+          mt = fmaxf(mt, hmax[(g * kHalves + (hf ^ 1)) * 128 + row]);
+        }
 
         // ---- running maximum, handed over from the previous tile's group
         float m_prev = -INFINITY;
@@ -756,7 +904,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           m_k = mt;
           resc = true;
         }
-        mpub[(k & 1) * 128 + row] = m_k;
+        // every warp of the group arrives once it has read m_prev, so the
+        // next writer of this slot (tile k + 1's group) cannot overwrite it early
+        if (hf == 0) mpub[(k & 1) * 128 + row] = m_k;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_MREADY + (k & 1)));
         if (m_g != m_k) {
@@ -764,10 +914,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           m_g = m_k;
         }
 
-        // ---- P (bf16 pairs) in registers first, packed in place into r[0..31]
+        // ---- P (bf16 pairs) in registers first, packed in place into r[0..kCols/2)
         float psum = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < kCols / 2; ++e) {
           const float p0 = ex2(__uint_as_float(r[2 * e]) - m_k);
           const float p1 = ex2(__uint_as_float(r[2 * e + 1]) - m_k);
           psum += p0 + p1;
@@ -781,13 +931,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (k >= 2 && !warp_wait(bar(BAR_O_DONE + ((k - 2) & 3)), ((k - 2) >> 2) & 1)) { ok = false; break; }
         if (group_lead) MLA_TR(k, 7);
 
-        // ---- rescale O between P(k-1) C and P(k) C (rare)
+        // ---- rescale O between P(k-1) C and P(k) C (rare); each half takes
+        // its share of the 16 chunks of 16 columns
         if (__any_sync(0xffffffffu, resc)) {
           const int kp = k - 1;
           if (!warp_wait(bar(BAR_O_DONE + (kp & 3)), (kp >> 2) & 1)) { ok = false; break; }
           tc_fence_after();
           const float alpha = resc ? exp2f(m_prev - m_k) : 1.0f;
-          for (int c = 0; c < 16; ++c) {
+          for (int c = (16 / kHalves) * hf; c < (16 / kHalves) * (hf + 1); ++c) {
             uint32_t v[16];
             tmem_ld16(tl + kColO + 16 * c, v);
             tmem_wait_ld();
@@ -797,9 +948,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           }
         }
         tc_fence_after();
-        const uint32_t pcol = kColP + 32 * (k & 1);
-        tmem_st16(tl + pcol, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
-        tmem_st16(tl + pcol + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
+        const uint32_t pcol = kColP + 32 * (k & 1) + (kCols / 2) * hf;
+#pragma unroll
+        for (int c = 0; c < kCols / 32; ++c)
+          tmem_st16(tl + pcol + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * c]));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -808,38 +960,51 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       }
 
       if (last) {
-        // ---- end of a segment: both groups
-        float2* ls = lstate + (seg & 1) * (kGroups * 128);
-        ls[g * 128 + row] = make_float2(m_g, l_g);
+        // ---- end of a segment: every softmax warp
+        float* lms = lm + (seg & 1) * (kGroups * 128);
+        float* lss = lsum + (seg & 1) * (kGroups * kHalves * 128);
+        if (hf == 0) lms[g * 128 + row] = m_g;
+        lss[(g * kHalves + hf) * 128 + row] = l_g;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_SEG));
         if (!warp_wait(bar(BAR_SEG), seg & 1)) { ok = false; break; }
+        if (group_lead && g == 0) MLA_TR(k, 12);
         float M = -INFINITY;
 #pragma unroll
-        for (int gg = 0; gg < kGroups; ++gg) M = fmaxf(M, ls[gg * 128 + row].x);
+        for (int gg = 0; gg < kGroups; ++gg) M = fmaxf(M, lms[gg * 128 + row]);
         float l = 0.f;
 #pragma unroll
         for (int gg = 0; gg < kGroups; ++gg) {
-          const float2 o = ls[gg * 128 + row];
-          if (o.x != -INFINITY) l += o.y * exp2f(o.x - M);
+          const float mg = lms[gg * 128 + row];
+          if (mg != -INFINITY) {
+            float lg = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < kHalves; ++hh) lg += lss[(gg * kHalves + hh) * 128 + row];
+            l += lg * exp2f(mg - M);
+          }
         }
         const int b = it.b;
-        // query of the next segment first: the MMA warp issues the last P.C
-        // of this segment only after the next segment's first score MMA
+        // query of the next segment first: the next score MMA can start while
+        // this segment's output is read out
         if (k + 1 < ntiles) {
           TileIter nx = it;
           nx.next();
           if (!warp_wait(bar(BAR_Q_FREE), seg & 1)) { ok = false; break; }
           tc_fence_after();
           load_q(nx.b);
+          if (group_lead && g == 0) MLA_TR(k, 13);
         }
-        // epilogue: O_r / l -> o_part slot (part + b); this group's 128 columns
+        // epilogue: O_r / l -> o_part slot (part + b); 16 chunks of 16 columns
+        // split between the softmax threads of the row
         if (!warp_wait(bar(BAR_O_DONE + (k & 3)), (k >> 2) & 1)) { ok = false; break; }
+        if (group_lead && g == 0) MLA_TR(k, 14);
         tc_fence_after();
         const int64_t slot = (int64_t)part + b;
         float* orow = p.o_part + (slot * p.h + row) * 512 + rank * 256;
         const float inv = 1.0f / l;
-        for (int c = (16 * g) / kGroups; c < (16 * (g + 1)) / kGroups; ++c) {
+        constexpr int kEpiChunks = 16 / (kGroups * kHalves);
+        const int ec0 = (g * kHalves + hf) * kEpiChunks;
+        for (int c = ec0; c < ec0 + kEpiChunks; ++c) {
           uint32_t v[16];
           tmem_ld16(tl + kColO + 16 * c, v);
           tmem_wait_ld();
@@ -851,17 +1016,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
                               __uint_as_float(v[4 * q4 + 2]) * inv, __uint_as_float(v[4 * q4 + 3]) * inv);
           }
         }
-        if (live && rank == 0 && g == 0) p.lse_part[slot * p.h + row] = (M + log2f(l)) * kLn2;
+        if (live && rank == 0 && g == 0 && hf == 0) p.lse_part[slot * p.h + row] = (M + log2f(l)) * kLn2;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_O_FREE));
+        if (group_lead && g == 0) MLA_TR(k, 15);
         m_g = -INFINITY;
         l_g = 0.f;
         ++seg;
       }
       if (k + 1 < ntiles) it.next();
     }
-    if (!ok) fail();
+    if (!ok) {
+      fail();
+      // the partner warp of this lane quarter may be held at one of the two
+      // pair meetings of a tile: arrive twice so that it reaches a wait that
+      // sees the abort flag
+      if constexpr (kHalves > 1) {
+        asm volatile("bar.arrive %0, 64;" ::"r"(1 + 4 * g + sub) : "memory");
+        asm volatile("bar.arrive %0, 64;" ::"r"(1 + 4 * g + sub) : "memory");
+      }
+    }
   }
 
   // teardown: TMEM free after every reader is done; the cluster stays up until
