@@ -65,6 +65,9 @@ constexpr int kHalves = 2;
 constexpr int kCols = 64 / kHalves;         // score columns per softmax thread
 constexpr int kGroupWarps = 4 * kHalves;
 constexpr int kSoftWarps = kGroups * kGroupWarps;
+// 1: the softmax warps poll for their scores without suspending (faster
+// wake-up, at the cost of issue slots the other group's warps could use)
+constexpr int kSpinSoftmax = 1;
 constexpr int kBoxBytes = 64 * 128;         // 64 rows x 64 bf16, 128-byte swizzle
 constexpr int kRopeBoxBytes = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
 constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // 4 latent boxes + half the RoPE dims
@@ -158,6 +161,51 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 32-byte global accesses (sm_100 family): one sector per thread, half the
+// instructions of 16-byte ones; the address must be 32-byte aligned
+__device__ __forceinline__ void ldg_nc_v8(const void* ptr, uint32_t* w) {
+  asm volatile("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(ptr));
+}
+__device__ __forceinline__ void stg_v8(void* ptr, const float* v) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "f"(v[0]),
+               "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
+// packed pairs of float32 (lo, hi) for the sm_100-family f32x2 arithmetic
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2_make(float lo, float hi) {
+  f2_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f2_split(f2_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+  f2_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
+  f2_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+  f2_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+  f2_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -167,12 +215,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // -DMLA_TRACE; the product build has none of it).
 #ifdef MLA_TRACE
 constexpr int kTraceTiles = 128;
-constexpr int kTraceEv = 16;
+constexpr int kTraceEv = 24;
 __device__ unsigned long long* g_trace = nullptr;
 #define MLA_TR(k, ev)                                                                   \
   do {                                                                                  \
     if (g_trace != nullptr && part < 2 && (k) < kTraceTiles)                            \
       g_trace[((part * 2 + rank) * kTraceTiles + (k)) * kTraceEv + (ev)] = clock64();   \
+  } while (0)
+#define MLA_TRMAX(k, ev)                                                                \
+  do {                                                                                  \
+    if (g_trace != nullptr && part < 2 && (k) < kTraceTiles)                            \
+      atomicMax(&g_trace[((part * 2 + rank) * kTraceTiles + (k)) * kTraceEv + (ev)],    \
+                (unsigned long long)clock64());                                         \
+  } while (0)
+#define MLA_TRMIN(k, ev)                                                                \
+  do {                                                                                  \
+    if (g_trace != nullptr && part < 2 && (k) < kTraceTiles)                            \
+      atomicMax(&g_trace[((part * 2 + rank) * kTraceTiles + (k)) * kTraceEv + (ev)],    \
+                ~(unsigned long long)clock64());                                        \
   } while (0)
 #define MLA_SITE(site)                                                                  \
   do {                                                                                  \
@@ -182,6 +242,12 @@ __device__ unsigned long long* g_trace = nullptr;
 #else
 #define MLA_TR(k, ev) \
   do {                \
+  } while (0)
+#define MLA_TRMAX(k, ev) \
+  do {                   \
+  } while (0)
+#define MLA_TRMIN(k, ev) \
+  do {                   \
   } while (0)
 #define MLA_SITE(site) \
   do {                 \
@@ -323,6 +389,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     }
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   };
+  // the same for the MMA issuer warps, polling without suspending
+  auto warp_spin = [&](uint32_t b, uint32_t parity) -> bool {
+    bool ok = true;
+    if (lane == 0) {
+      ok = mbar_spin_or_abort(b, parity, lim, abort_flag, &timed_out);
+      if (!ok && timed_out) MLA_SITE(1000 + warp * 100 + (int)((b - bar(0)) / 8));
+    }
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  };
   auto warp_wait_cluster = [&](uint32_t b, uint32_t parity) -> bool {
     bool ok = true;
     if (lane == 0) {
@@ -370,7 +445,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (*abort_flag) break;
         const int st = k % kStages;
         if (k >= kStages &&
-            !mbar_wait_or_abort(bar(BAR_KV_EMPTY + st), ((k / kStages) - 1) & 1, lim, abort_flag,
+            !mbar_spin_or_abort(bar(BAR_KV_EMPTY + st), ((k / kStages) - 1) & 1, lim, abort_flag,
                                 &timed_out)) {
           fail();
           break;
@@ -441,10 +516,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       const int st = ks % kStages;
       const bool first = (ks == 0) || (its.blk == 0);
       const bool last = (ks == ntiles - 1) || (its.blk == its.nb - 1);
-      if (first && !warp_wait(bar(BAR_Q_READY), seg_s & 1)) { ok = false; break; }
-      if (!warp_wait(bar(BAR_KV_FULL + st), (ks / kStages) & 1)) { ok = false; break; }
-      if (ks > 0 && !warp_wait(bar(BAR_S_EMPTY), (ks - 1) & 1)) { ok = false; break; }
+      // the tile's length first: its global load then overlaps the waits
       const int n_valid = its.valid();
+      if (first && !warp_spin(bar(BAR_Q_READY), seg_s & 1)) { ok = false; break; }
+      if (!warp_spin(bar(BAR_KV_FULL + st), (ks / kStages) & 1)) { ok = false; break; }
+      if (lane == 0) MLA_TR(ks, 16);
+      if (ks > 0 && !warp_spin(bar(BAR_S_EMPTY), (ks - 1) & 1)) { ok = false; break; }
+      if (lane == 0) MLA_TR(ks, 17);
       if (n_valid < kTok) {
         // slots past the sequence end: zero them so that P = 0 meets finite values
         uint8_t* sp = smem + kOffStages + st * kStageBytes;
@@ -502,8 +580,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     for (int ko = 0; ko < ntiles; ++ko) {
       const bool first = (ko == 0) || (ito.blk == 0);
       const bool last = (ko == ntiles - 1) || (ito.blk == ito.nb - 1);
-      if (first && seg_o > 0 && !warp_wait(bar(BAR_O_FREE), (seg_o - 1) & 1)) { ok = false; break; }
-      if (!warp_wait(bar(BAR_P_FULL + (ko & 1)), (ko >> 1) & 1)) { ok = false; break; }
+      if (first && seg_o > 0 && !warp_spin(bar(BAR_O_FREE), (seg_o - 1) & 1)) { ok = false; break; }
+      if (!warp_spin(bar(BAR_P_FULL + (ko & 1)), (ko >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
         MLA_TR(ko, 2);
@@ -541,6 +619,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     its.init(p.seq_lens, p.max_blocks, b_first, blk_first);
     ito.init(p.seq_lens, p.max_blocks, b_first, blk_first);
     int ks = 0, ko = 0, seg_s = 0, seg_o = 0;
+    int nv_s = its.valid();  // valid tokens of tile ks
     long long idle_since = clock64();
     bool ok = true;
     // lane 0: issue O(ko) if its P is ready (state is advanced by advance_o on all lanes)
@@ -601,7 +680,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           ready = q_ok && kv_ok && s_ok;
         }
         if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) {
-          const int n_valid = its.valid();
+          const int n_valid = nv_s;
           if (n_valid < kTok) {
             // slots past the sequence end: zero them so that P = 0 meets finite values
             uint8_t* sp = smem + kOffStages + st * kStageBytes;
@@ -642,7 +721,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           if (__shfl_sync(0xffffffffu, o_issued_inside ? 1 : 0, 0)) advance_o();
           __syncwarp();
           if (last) ++seg_s;
-          if (ks + 1 < ntiles) its.next();
+          if (ks + 1 < ntiles) {
+            its.next();
+            nv_s = its.valid();  // loaded now, needed only at the next score MMA
+          }
           ++ks;
           did = true;
         }
@@ -751,6 +833,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     // memory); the eight 16-column chunks (32 dims each) are split between
     // the softmax threads of a row.
     constexpr int kQChunks = 8 / (kGroups * kHalves);
+    // 32-byte accesses need 32-byte aligned bases (the interface asks for 16)
+    const bool q32 = (reinterpret_cast<uintptr_t>(p.q_cat) & 31u) == 0;
+    const bool o32 = (reinterpret_cast<uintptr_t>(p.o_part) & 31u) == 0;
     static_assert(kQChunks * kGroups * kHalves == 8, "query chunks per thread");
     auto load_q = [&](int b) {
       if (group_lead && g == 0) {
@@ -760,18 +845,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       }
       const uint4* q = reinterpret_cast<const uint4*>(p.q_cat + ((int64_t)b * p.h + (live ? row : 0)) * 576);
       const int qc0 = (g * kHalves + hf) * kQChunks;
-      // all loads first (one memory round trip), then the TMEM stores
+      // all loads first (one memory round trip), then the TMEM stores; rows
+      // are 1152 bytes apart, so each load instruction touches 32 lines:
+      // 32-byte loads where q_cat allows them halve that traffic
       uint32_t w[kQChunks][16];
 #pragma unroll
       for (int cc = 0; cc < kQChunks; ++cc) {
         const int dim0 = 256 * (int)rank + 32 * (qc0 + cc);
+        if (!live) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 v = live ? __ldg(q + dim0 / 8 + u) : make_uint4(0, 0, 0, 0);
-          w[cc][4 * u + 0] = v.x;
-          w[cc][4 * u + 1] = v.y;
-          w[cc][4 * u + 2] = v.z;
-          w[cc][4 * u + 3] = v.w;
+          for (int e = 0; e < 16; ++e) w[cc][e] = 0u;
+        } else if (q32) {
+          ldg_nc_v8(q + dim0 / 8, &w[cc][0]);
+          ldg_nc_v8(q + dim0 / 8 + 2, &w[cc][8]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 v = __ldg(q + dim0 / 8 + u);
+            w[cc][4 * u + 0] = v.x;
+            w[cc][4 * u + 1] = v.y;
+            w[cc][4 * u + 2] = v.z;
+            w[cc][4 * u + 3] = v.w;
+          }
         }
       }
 #pragma unroll
@@ -797,8 +892,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         const int u = k / kGroups;  // use index of this group's exchange buffers
         const int n_valid = it.valid();
         // ---- partial scores of this CTA, this thread's columns
-        if (!warp_wait(bar(BAR_S_FULL + g), u & 1)) { ok = false; break; }
+        if (!(kSpinSoftmax ? warp_spin(bar(BAR_S_FULL + g), u & 1)
+                           : warp_wait(bar(BAR_S_FULL + g), u & 1))) { ok = false; break; }
         if (group_lead) MLA_TR(k, 3);
+        if (lane == 0) { MLA_TRMAX(k, 19); MLA_TRMIN(k, 20); }
         tc_fence_after();
         uint32_t r[kCols];
 #pragma unroll
@@ -808,7 +905,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (group_lead) MLA_TR(k, 9);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_S_EMPTY));
+        if (lane == 0) { MLA_TRMAX(k, 18); mbar_arrive(bar(BAR_S_EMPTY)); }
 
         // ---- exchange with the peer CTA
         // (no data comes back with this signal, so a CTA-scope wait suffices)
@@ -857,16 +954,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (group_lead) MLA_TR(k, 5);
         // full score (log2 domain) in place: r <- (own partial + peer's) * scale
         float mt = -INFINITY;
+        const f2_t scale2 = f2_make(p.scale_log2, p.scale_log2);
 #pragma unroll
         for (int c = 0; c < kMyChunks; ++c) {
           const uint4 v = *reinterpret_cast<const uint4*>(my_recv + c * 512);
           const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
+          for (int e = 0; e < 4; e += 2) {
             const int kk = 4 * c + e;
-            const float xs =
-                (__uint_as_float(r[kk]) + __uint_as_float(vv[e] & 0xFFFFFF00u)) * p.scale_log2;
-            r[kk] = __float_as_uint(xs);
+            const f2_t own = f2_make(__uint_as_float(r[kk]), __uint_as_float(r[kk + 1]));
+            const f2_t oth = f2_make(__uint_as_float(vv[e] & 0xFFFFFF00u),
+                                     __uint_as_float(vv[e + 1] & 0xFFFFFF00u));
+            float x0, x1;
+            f2_split(f2_mul(f2_add(own, oth), scale2), x0, x1);
+            r[kk] = __float_as_uint(x0);
+            r[kk + 1] = __float_as_uint(x1);
           }
         }
         // the buffer may be refilled: tell the peer (the values are consumed)
@@ -915,15 +1017,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         }
 
         // ---- P (bf16 pairs) in registers first, packed in place into r[0..kCols/2)
-        float psum = 0.f;
+        f2_t psum2 = f2_make(0.f, 0.f);
+        const f2_t negm = f2_make(-m_k, -m_k);
 #pragma unroll
         for (int e = 0; e < kCols / 2; ++e) {
-          const float p0 = ex2(__uint_as_float(r[2 * e]) - m_k);
-          const float p1 = ex2(__uint_as_float(r[2 * e + 1]) - m_k);
-          psum += p0 + p1;
+          const f2_t y = f2_add(f2_make(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), negm);
+          float y0, y1;
+          f2_split(y, y0, y1);
+          const float p0 = ex2(y0), p1 = ex2(y1);
+          psum2 = f2_add(psum2, f2_make(p0, p1));
           r[e] = pack_bf16x2(p0, p1);
         }
-        l_g += psum;
+        {
+          float s0, s1;
+          f2_split(psum2, s0, s1);
+          l_g += s0 + s1;
+        }
 
         // ---- P buffer (k & 1) was read by the P.C MMA of tile k-2; waiting for it
         // also makes O(k-3) complete, so the rescale's wait on the other group's
@@ -955,7 +1064,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_P_FULL + (k & 1)));
+        if (lane == 0) { MLA_TRMAX(k, 21); mbar_arrive(bar(BAR_P_FULL + (k & 1))); }
         if (group_lead) MLA_TR(k, 8);
       }
 
@@ -1009,11 +1118,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           tmem_ld16(tl + kColO + 16 * c, v);
           tmem_wait_ld();
           if (live) {
+            float o[16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              *reinterpret_cast<float4*>(orow + 16 * c + 4 * q4) =
-                  make_float4(__uint_as_float(v[4 * q4]) * inv, __uint_as_float(v[4 * q4 + 1]) * inv,
-                              __uint_as_float(v[4 * q4 + 2]) * inv, __uint_as_float(v[4 * q4 + 3]) * inv);
+            for (int e = 0; e < 16; ++e) o[e] = __uint_as_float(v[e]) * inv;
+            if (o32) {
+              stg_v8(orow + 16 * c, o);
+              stg_v8(orow + 16 * c + 8, o + 8);
+            } else {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                *reinterpret_cast<float4*>(orow + 16 * c + 4 * q4) =
+                    make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+            }
           }
         }
         if (live && rank == 0 && g == 0 && hf == 0) p.lse_part[slot * p.h + row] = (M + log2f(l)) * kLn2;

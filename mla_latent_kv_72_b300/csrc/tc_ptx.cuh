@@ -132,6 +132,28 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
   }
 }
 
+// The same bound and abort rule, polling with test_wait, which never suspends
+// the thread: a suspended try_wait can resume hundreds of cycles after the
+// phase completes.  For warps with nothing else to do whose wake-up sits on
+// the pipeline's critical path (the MMA issuers); one poll every few tens of
+// cycles costs the warps sharing the sub-partition little issue bandwidth.
+__device__ __forceinline__ bool mbar_spin_or_abort(uint32_t bar, uint32_t parity,
+                                                   long long limit_cycles,
+                                                   const volatile int* abort, bool* timed_out) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort) return false;
+      if (clock64() - t0 > limit_cycles) {
+        *timed_out = true;
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // cluster / distributed shared memory
 // ---------------------------------------------------------------------------
