@@ -55,7 +55,7 @@ using namespace tc;
 
 constexpr int kTok = 64;                    // tokens per tile (= cache block)
 constexpr int kMaxStages = 4;              // stage count of the bf16 variant (the larger)
-constexpr int kPrefetch = 6;                // tiles prefetched into L2 beyond the stages
+constexpr int kPrefetch = 0;                // tiles prefetched into L2 beyond the stages
 constexpr int kLandBytes = 64 * 256;        // FP8 variant: 64 tokens x 256 e4m3 codes
 constexpr int kGroups = 2;                  // softmax groups (tile k goes to group k % kGroups)
 // warps per TMEM lane quarter in a softmax group: with 2, a row's 64 scores are
@@ -413,8 +413,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       TileIter it;
       it.init(p.seq_lens, p.max_blocks, b_first, blk_first);
       const uint32_t tx = kStageBytes;
-      // L2 prefetch runs kPrefetch tiles ahead of the loads, so that a stage
-      // freed late (after its P.C MMA) refills from L2 rather than HBM
+      // L2 prefetch of the tiles whose loads come in the next kStages
+      // iterations (plus kPrefetch more), so that a stage freed late (after
+      // its P.C MMA) refills from L2 rather than HBM; running further ahead
+      // lets the cache stream evict prefetched lines before their load, which
+      // then reads them from HBM a second time
       TileIter pf;
       pf.init(p.seq_lens, p.max_blocks, b_first, blk_first);
       int kp = 0;
@@ -929,6 +932,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         {
           const long long t0 = clock64();
           bool got = false;
+          // watch one chunk until it carries the tag (one load per round),
+          // then check them all
+          while (true) {
+            uint32_t v0, v1, v2, v3;
+            asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                         : "r"(my_recv_u32 + (kMyChunks - 1) * 512)
+                         : "memory");
+            const bool seen = ((v0 & 0xFFu) == tag) & ((v1 & 0xFFu) == tag) &
+                              ((v2 & 0xFFu) == tag) & ((v3 & 0xFFu) == tag);
+            if (__all_sync(0xffffffffu, seen)) break;
+            if (*abort_flag || clock64() - t0 > lim) break;
+          }
           while (true) {
             bool mine = true;
 #pragma unroll
