@@ -55,7 +55,7 @@ using namespace tc;
 
 constexpr int kTok = 64;                    // tokens per tile (= cache block)
 constexpr int kMaxStages = 4;              // stage count of the bf16 variant (the larger)
-constexpr int kPrefetch = 0;                // tiles prefetched into L2 beyond the stages
+constexpr int kPrefetchAhead = 1;           // L2 prefetch: tiles ahead of the TMA load
 constexpr int kLandBytes = 64 * 256;        // FP8 variant: 64 tokens x 256 e4m3 codes
 constexpr int kGroups = 2;                  // softmax groups (tile k goes to group k % kGroups)
 // warps per TMEM lane quarter in a softmax group: with 2, a row's 64 scores are
@@ -67,7 +67,7 @@ constexpr int kGroupWarps = 4 * kHalves;
 constexpr int kSoftWarps = kGroups * kGroupWarps;
 // 1: the softmax warps poll for their scores without suspending (faster
 // wake-up, at the cost of issue slots the other group's warps could use)
-constexpr int kSpinSoftmax = 1;
+constexpr int kSpinSoftmax = 0;
 constexpr int kBoxBytes = 64 * 128;         // 64 rows x 64 bf16, 128-byte swizzle
 constexpr int kRopeBoxBytes = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
 constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // 4 latent boxes + half the RoPE dims
@@ -413,11 +413,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       TileIter it;
       it.init(p.seq_lens, p.max_blocks, b_first, blk_first);
       const uint32_t tx = kStageBytes;
-      // L2 prefetch of the tiles whose loads come in the next kStages
-      // iterations (plus kPrefetch more), so that a stage freed late (after
-      // its P.C MMA) refills from L2 rather than HBM; running further ahead
-      // lets the cache stream evict prefetched lines before their load, which
-      // then reads them from HBM a second time
+      // L2 prefetch of the tiles whose loads come next (kPrefetchAhead tiles
+      // ahead of the load), so that a stage freed late (after its P.C MMA)
+      // refills partly from L2; running further ahead lets the cache stream
+      // evict prefetched lines before their load, which then reads them from
+      // HBM a second time
       TileIter pf;
       pf.init(p.seq_lens, p.max_blocks, b_first, blk_first);
       int kp = 0;
@@ -444,7 +444,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       };
       int k = 0;
       for (; k < ntiles; ++k) {
-        prefetch_upto(k + kStages + kPrefetch);
+        prefetch_upto(k + 1 + kPrefetchAhead);
         if (*abort_flag) break;
         const int st = k % kStages;
         if (k >= kStages &&
