@@ -49,10 +49,10 @@ struct GemmParams {
   void* out;        // element (b, s, m) at out + (b * h + s) * out_ld + m
   int out_ld;
   int out_dtype;
-  // rotary part of the absorbed query (absorb only, m tile 0)
+  // rotary part of the absorbed query (absorb only)
   const uint16_t* q_rope;  // [B, h, 64] bf16 or null
   const int32_t* q_pos;
-  double theta;
+  double inv_freq[32];     // theta^(-2i/64), formed in float64 on the host
   int32_t* status;
   long long wait_limit;
 };
@@ -144,17 +144,16 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
   }
   __syncwarp();
 
-  // rotary query part (absorb, m tile 0): independent of the MMA
-  if (p.q_rope != nullptr && mt == 0) {
-    __shared__ double inv_freq[32];
-    if (threadIdx.x < 32) inv_freq[threadIdx.x] = pow(p.theta, -2.0 * (double)threadIdx.x / 64.0);
-    __syncthreads();
+  // rotary query part (absorb): independent of the MMA; the (row, pair) items
+  // of this head are spread over its m-tile CTAs, since the float64 angle
+  // reduction runs on the slow FP64 pipe
+  if (p.q_rope != nullptr) {
     const int nb = min(p.n_tile, p.B - b0);
     uint16_t* q_cat = static_cast<uint16_t*>(p.out);
-    for (int i = threadIdx.x; i < nb * 32; i += kGThreads) {
+    for (int i = threadIdx.x + mt * kGThreads; i < nb * 32; i += kGThreads * (int)gridDim.y) {
       const int bb = b0 + i / 32, pr = i % 32;
       float cs, sn;
-      rope_cos_sin((double)p.q_pos[bb], inv_freq[pr], &cs, &sn);
+      rope_cos_sin((double)p.q_pos[bb], p.inv_freq[pr], &cs, &sn);
       const int64_t ib = ((int64_t)bb * p.h + s) * 64;
       const float x0 = bf16_to_f32(p.q_rope[ib + 2 * pr]);
       const float x1 = bf16_to_f32(p.q_rope[ib + 2 * pr + 1]);
@@ -179,6 +178,26 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
       uint32_t v[16];
       tmem_ld16(tl + c0, v);
       tmem_wait_ld();
+      if (p.out_dtype == MLA_BF16) {
+        // pairs of neighbouring m (lanes 2j, 2j+1) as one 4-byte store: the
+        // even lane stores row e, the odd lane row e + 1
+        uint16_t* out16 = static_cast<uint16_t*>(p.out);
+        const bool odd = (lane & 1) != 0;
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const float send = __uint_as_float(odd ? v[e] : v[e + 1]);
+          const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+          const int b = b0 + c0 + e + (odd ? 1 : 0);
+          if (b < p.B) {
+            const float lo = odd ? recv : __uint_as_float(v[e]);
+            const float hi = odd ? __uint_as_float(v[e + 1]) : recv;
+            const int64_t o = ((int64_t)b * p.h + s) * p.out_ld + mt * 128 + (m & ~1);
+            *reinterpret_cast<uint32_t*>(out16 + o) =
+                (uint32_t)f32_to_bf16_rn(lo) | ((uint32_t)f32_to_bf16_rn(hi) << 16);
+          }
+        }
+        continue;
+      }
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int b = b0 + c0 + e;
@@ -273,7 +292,7 @@ cudaError_t launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int
   p.out_dtype = MLA_BF16;
   p.q_rope = static_cast<const uint16_t*>(q_rope);
   p.q_pos = q_pos;
-  p.theta = theta;
+  for (int i = 0; i < 32; ++i) p.inv_freq[i] = pow(theta, -2.0 * (double)i / 64.0);
   p.status = nullptr;
   p.wait_limit = 4000000000LL;
   dim3 grid(h, 512 / 128, ceil_div(B, nt));
@@ -306,7 +325,6 @@ cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, i
   p.out_dtype = out_dtype;
   p.q_rope = nullptr;
   p.q_pos = nullptr;
-  p.theta = 0.0;
   p.status = nullptr;
   p.wait_limit = 4000000000LL;
   dim3 grid(h, 1, ceil_div(B, nt));
