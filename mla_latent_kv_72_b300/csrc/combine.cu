@@ -17,8 +17,8 @@ constexpr int kThreads = 32 * kHeadsPerCta;
 constexpr int kMaxSplits = 1024;
 
 // grid: (ceil(h / kHeadsPerCta), B); warp w merges head blockIdx.x * 8 + w of
-// sequence blockIdx.y.  Lane l owns latent columns 4l + 128 j (16-byte loads,
-// each warp access a contiguous 512-byte run).
+// sequence blockIdx.y.  Lane l owns latent columns 4l + 128 i of each
+// 512-column run (16-byte loads, each warp access a contiguous 512-byte run).
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                const int32_t* __restrict__ seq_lens, int bs, int max_blocks, int B, int h,
@@ -64,27 +64,54 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 
   const int64_t obase = ((int64_t)b * h + s) * d_c;
-  for (int c = 4 * lane; c < d_c; c += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < count; ++j) {
-      const float l = lse_col[(int64_t)j * h];
-      const float w = (m == -INFINITY || l == -INFINITY) ? 0.f : expf(l - m);
-      if (w == 0.f) continue;
-      const float4 v = *reinterpret_cast<const float4*>(o_part + (((int64_t)first + j) * h + s) * d_c + c);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+  // lane j of each round of 32 splits holds split j's weight; every split's
+  // loads go out without waiting on its weight (a zero weight, an empty
+  // split, is applied by select, so whatever its slot holds is ignored)
+  for (int c0 = 0; c0 < d_c; c0 += 512) {
+    float4 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < count; j0 += 32) {
+      float wl = 0.f;
+      if (j0 + lane < count) {
+        const float l = lse_col[(int64_t)(j0 + lane) * h];
+        wl = (m == -INFINITY || l == -INFINITY) ? 0.f : expf(l - m);
+      }
+      const int n = count - j0 < 32 ? count - j0 : 32;
+#pragma unroll 2
+      for (int jj = 0; jj < n; ++jj) {
+        const float w = __shfl_sync(0xffffffffu, wl, jj);
+        const float* src = o_part + (((int64_t)first + j0 + jj) * h + s) * d_c + c0 + 4 * lane;
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          v[i] = (c0 + 4 * lane + 128 * i < d_c) ? *reinterpret_cast<const float4*>(src + 128 * i)
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (w != 0.f) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[i].x = fmaf(w, v[i].x, acc[i].x);
+            acc[i].y = fmaf(w, v[i].y, acc[i].y);
+            acc[i].z = fmaf(w, v[i].z, acc[i].z);
+            acc[i].w = fmaf(w, v[i].w, acc[i].w);
+          }
+        }
+      }
     }
-    if (o_dtype == MLA_F32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(o_lat) + obase + c) =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    } else {
-      uint16_t* o = static_cast<uint16_t*>(o_lat) + obase + c;
-      uint2 pk;
-      pk.x = (uint32_t)f32_to_bf16_rn(acc.x * inv) | ((uint32_t)f32_to_bf16_rn(acc.y * inv) << 16);
-      pk.y = (uint32_t)f32_to_bf16_rn(acc.z * inv) | ((uint32_t)f32_to_bf16_rn(acc.w * inv) << 16);
-      *reinterpret_cast<uint2*>(o) = pk;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = c0 + 4 * lane + 128 * i;
+      if (c >= d_c) continue;
+      if (o_dtype == MLA_F32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(o_lat) + obase + c) =
+            make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
+      } else {
+        uint16_t* o = static_cast<uint16_t*>(o_lat) + obase + c;
+        uint2 pk;
+        pk.x = (uint32_t)f32_to_bf16_rn(acc[i].x * inv) | ((uint32_t)f32_to_bf16_rn(acc[i].y * inv) << 16);
+        pk.y = (uint32_t)f32_to_bf16_rn(acc[i].z * inv) | ((uint32_t)f32_to_bf16_rn(acc[i].w * inv) << 16);
+        *reinterpret_cast<uint2*>(o) = pk;
+      }
     }
   }
   if (lse_out && lane == 0)
