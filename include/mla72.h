@@ -24,6 +24,10 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     never allocates, frees or synchronises.  Arrays are dense, row-major, in
  *     the shapes stated (last index fastest).
+ *   - Tensor pointers and row strides must be 16-byte aligned (MLA_ERR_ALIGN
+ *     otherwise).  When q_cat and o_part are 32-byte aligned (as every
+ *     cudaMalloc or PyTorch allocation is), the tensor-core decode moves them
+ *     with 32-byte accesses; otherwise with 16-byte ones, same results.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   - Host-side argument checks run before anything is launched; on failure
  *     the call returns a negative mla_status and launches nothing.
