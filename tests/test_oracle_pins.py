@@ -420,3 +420,112 @@ def test_variable_lengths_within_range():
     assert lens.min() >= 1024 and lens.max() <= 32768
     table, nblk = mi.block_table(w, lens)
     assert nblk == int(((lens + 63) // 64).sum())
+
+
+# ----------------------------------------------------------------------------
+# the oracle's per-step helpers that the GPU tests use as checkers
+# ----------------------------------------------------------------------------
+
+def test_absorb_query_equals_scalar_loops():
+    # kexue.fm "Part 1": q k^T = x (W_q W_k^T) c^T, so the absorbed latent query
+    # of head s is q_nope^(s) W_UK^(s): q_abs[c] = sum_d q_nope[d] w_uk[s, d, c].
+    # The RoPE part is the interleaved 2x2 rotation of each pair by q_pos * omega_i,
+    # written out with math.cos / math.sin (d_nope != d_c, B != h, so a swapped
+    # index or a mis-broadcast position changes the result or fails on shape)
+    rng = np.random.default_rng(21)
+    B, h, d_nope, d_c, d_r = 3, 2, 5, 7, 6
+    qn = rng.standard_normal((B, h, d_nope))
+    qr = rng.standard_normal((B, h, d_r))
+    wuk = rng.standard_normal((h, d_nope, d_c))
+    q_pos = np.array([0, 5, 1234])
+    got = O.absorb_query(qn, qr, q_pos, wuk)
+    assert got.shape == (B, h, d_c + d_r)
+    theta = 10000.0
+    for b in range(B):
+        for s in range(h):
+            for c in range(d_c):
+                acc = 0.0
+                for d in range(d_nope):
+                    acc += qn[b, s, d] * wuk[s, d, c]
+                assert abs(got[b, s, c] - acc) <= 1e-12 * (1 + abs(acc))
+            for i in range(d_r // 2):
+                ang = float(q_pos[b]) * theta ** (-2.0 * i / d_r)
+                a, bb = qr[b, s, 2 * i], qr[b, s, 2 * i + 1]
+                want0 = a * math.cos(ang) - bb * math.sin(ang)
+                want1 = a * math.sin(ang) + bb * math.cos(ang)
+                assert abs(got[b, s, d_c + 2 * i] - want0) <= 1e-12
+                assert abs(got[b, s, d_c + 2 * i + 1] - want1) <= 1e-12
+
+
+def test_absorb_query_scores_equal_per_head_keys():
+    # the absorbed query dotted with raw latents equals the non-absorbed score
+    # q_nope . (c W_UK^(s)T), and its RoPE part dotted with the rotated key
+    # equals RoPE(q_r, t) . RoPE(k_r, i) (kexue.fm "Part 1" and "Part 2")
+    rng = np.random.default_rng(22)
+    B, h, d_nope, d_c, d_r, L = 2, 3, 6, 10, 4, 9
+    qn = rng.standard_normal((B, h, d_nope))
+    qr = rng.standard_normal((B, h, d_r))
+    wuk = rng.standard_normal((h, d_nope, d_c))
+    q_pos = np.array([8, 3])
+    c = rng.standard_normal((L, d_c))
+    kr = rng.standard_normal((L, d_r))
+    q_cat = O.absorb_query(qn, qr, q_pos, wuk)
+    for b in range(B):
+        for s in range(h):
+            k_c = c @ wuk[s].T                       # per-head content keys [L, d_nope]
+            np.testing.assert_allclose(q_cat[b, s, :d_c] @ c.T, k_c @ qn[b, s],
+                                       rtol=1e-12, atol=1e-12)
+            rel = q_cat[b, s, d_c:] @ O.rope(kr, np.arange(L)).T
+            want = [np.dot(O.rope_matrix(d_r, q_pos[b]).T @ qr[b, s],
+                           O.rope_matrix(d_r, i).T @ kr[i]) for i in range(L)]
+            np.testing.assert_allclose(rel, want, rtol=1e-12, atol=1e-12)
+
+
+def test_output_projection_equals_per_head_values():
+    # o_lat W_UV^(s)T must equal the output the non-absorbed reference forms from
+    # per-head values v_i = c_i W_UV^(s)T (kexue.fm "Part 1": W_v moves to the
+    # output side), and a scalar loop at tiny dims
+    rng = np.random.default_rng(23)
+    qn, qr, q_pos, wuk, wuv, seqs = _rand_case(rng, B=2, h=3, d_c=12, d_r=4, d_nope=5, d_v=7,
+                                               lens=(6, 11))
+    ref = O.decode_reference(qn, qr, q_pos, wuk, wuv, seqs)
+    np.testing.assert_allclose(O.output_projection(ref["o_lat"], wuv), ref["out"],
+                               rtol=1e-12, atol=1e-14)
+    o = rng.standard_normal((2, 3, 12))
+    got = O.output_projection(o, wuv)
+    for b in range(2):
+        for s in range(3):
+            for v in range(7):
+                acc = sum(o[b, s, c] * wuv[s, v, c] for c in range(12))
+                assert abs(got[b, s, v] - acc) <= 1e-12
+
+
+def test_quantized_latent_blocks_follow_the_rows():
+    # L = 130 rows: blocks [0, 64), [64, 128), [128, 130), each with its own
+    # magnitude, so an off-by-one block boundary changes some block's amax
+    rng = np.random.default_rng(24)
+    d_c = 32
+    x = rng.standard_normal((130, d_c)).astype(np.float32)
+    x[:64] *= np.float32(0.5)
+    x[64:128] *= np.float32(3.0)
+    x[128:] *= np.float32(40.0)
+    x[5, 3] = np.float32(9.0)           # block 0's amax sits inside the block
+    x[127, 0] = np.float32(-30.0)       # block 1's amax is its last row
+    x[128, 1] = np.float32(500.0)       # block 2's amax is its first row
+    codes, scales, deq = O.quantized_latent_f64(x, 64)
+    assert codes.shape == x.shape and scales.shape == (3,)
+    bounds = [(0, 64), (64, 128), (128, 130)]
+    want_amax = [9.0, 30.0, 500.0]
+    for j, (r0, r1) in enumerate(bounds):
+        blk = x[r0:r1]
+        assert float(np.abs(blk).max()) == want_amax[j]
+        assert scales[j] == np.float32(np.float32(want_amax[j]) / np.float32(448.0))
+        # every code of the block decodes to within half an e4m3 step of x / scale
+        q = (blk / scales[j]).astype(np.float64)
+        vals = O.e4m3_decode(codes[r0:r1])
+        assert np.all(np.abs(vals - q) <= np.maximum(np.abs(q) * 2.0 ** -4, 2.0 ** -10) + 1e-12)
+        np.testing.assert_array_equal(deq[r0:r1], vals * np.float64(scales[j]))
+    # the block's largest magnitude maps to the largest code, 448
+    assert O.e4m3_decode(codes[5, 3]) == 448.0
+    assert O.e4m3_decode(codes[127, 0]) == -448.0
+    assert O.e4m3_decode(codes[128, 1]) == 448.0
