@@ -1,11 +1,19 @@
 """Benchmark of one MLA absorbed-decode step on B300.
 
 One step = mla_absorb_q -> mla_decode_fwd -> mla_combine -> mla_out_proj over
-the DeepSeek-V3-shaped workload (B=64 sequences, h=128 heads, L=8192 cached
-tokens each, bf16, d_c=512, d_r=64), synthetic seeded inputs resident in HBM.
-Prints one JSON line (rank 0).
+one of the five seeded synthetic workloads (default: the DeepSeek-V3-shaped
+one, B=64 sequences, h=128 heads, L=8192 cached tokens each, bf16, d_c=512,
+d_r=64), inputs resident in HBM.  Prints one JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1..5 | NAME] [--parts P]
+
+Timing: the clock sampler starts first, then untimed steps run for
+--settle-s seconds (so that the SM and memory clocks sit at their loaded
+state), then W warm-up steps, then exactly K timed steps with no idle gap
+in between.  CUDA events bracket every decode launch; the line reports the
+mean, median and minimum of those per-launch times next to the whole-step
+throughput.
 
 The reference arm (--impl reference) times the float64 CPU oracle on the
 host cores on a bounded sample of the same workload.
@@ -24,10 +32,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-WORKLOAD = "v3_bf16_b64_h128_l8192"
+DEFAULT_WORKLOAD = "v3_bf16_b64_h128_l8192"
 METRIC = "MLA decode: latent-cache GB/s & TFLOP/s vs roofline (h=128, B=64, L=8k)"
 UNIT = "GB/s"
 PEAK_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+L2_BYTES = 126 * 1024 * 1024
 
 
 # ----------------------------------------------------------------------------
@@ -73,6 +82,27 @@ def load_peaks() -> tuple[dict, str]:
         return dict(PEAK_FALLBACK), "fallback"
 
 
+def roofline(alg_bytes: float, alg_flops: float, seconds: float, hbm_gbs: float,
+             tc_tflops: float) -> dict:
+    """Roofline of one kernel launch: the bound is the slower of moving its
+    algorithmic bytes at the HBM peak and doing its flops at the tensor peak;
+    frac = that bound's time / the measured time (= achieved / peak of the bound)."""
+    t_mem = alg_bytes / (hbm_gbs * 1e9)
+    t_tc = alg_flops / (tc_tflops * 1e12)
+    if t_mem >= t_tc:
+        achieved, peak, unit, bound = alg_bytes / seconds / 1e9, hbm_gbs, "GB/s", "hbm"
+    else:
+        achieved, peak, unit, bound = alg_flops / seconds / 1e12, tc_tflops, "TFLOP/s", "tensor"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "t_mem_us": t_mem * 1e6, "t_tensor_us": t_tc * 1e6}
+
+
+def step_stats(ms: list[float]) -> dict:
+    """Mean, median and minimum of per-launch times (milliseconds)."""
+    return {"mean_ms": statistics.fmean(ms), "median_ms": statistics.median(ms),
+            "min_ms": min(ms)}
+
+
 def parse_clock_csv(text: str) -> dict | None:
     """Median SM clock, max clock and the throttle reasons seen, from the
     nvidia-smi query recorded during the timed region."""
@@ -108,7 +138,8 @@ def parse_clock_csv(text: str) -> dict | None:
 
 
 class ClockSampler:
-    """nvidia-smi sampling of the SM clock and throttle reasons while running."""
+    """nvidia-smi sampling of the SM clock and throttle reasons while running
+    (reads only; nothing is set)."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -129,7 +160,6 @@ class ClockSampler:
                  "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
         return self
 
     def __exit__(self, *exc):
@@ -154,12 +184,15 @@ class ClockSampler:
                 pass
 
 
-def read_profile_traffic(kernel_sha: str) -> float | None:
-    """DRAM bytes per launch of the decode kernel from the committed ncu summary,
-    if it was taken on this exact kernel source."""
-    path = os.path.join(ROOT, "profiles", "decode_tc_v3_bf16_b64_h128_l8192.md")
+def profile_path(workload: str) -> str:
+    return os.path.join(ROOT, "profiles", f"decode_tc_{workload}.md")
+
+
+def read_profile_traffic(workload: str, kernel_sha: str) -> float | None:
+    """DRAM bytes per launch of the decode kernel on this workload from the
+    committed ncu summary, if it was taken on this exact kernel source."""
     try:
-        text = open(path).read()
+        text = open(profile_path(workload)).read()
     except OSError:
         return None
     sha = traffic = None
@@ -182,33 +215,27 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def resolve_workload(arg):
+    import mla_inputs as mi
+    if arg is None:
+        return mi.workload(DEFAULT_WORKLOAD)
+    if isinstance(arg, str) and arg.isdigit():
+        arg = int(arg)
+    return mi.workload(arg)
+
+
+def bench_config(w, num_parts, l2_note) -> dict:
+    return {"workload": w.name, "B": w.B, "h": w.h, "L": w.L,
+            "L_range": list(w.L_range) if w.L_range else None, "d_c": w.d_c, "d_r": w.d_r,
+            "d_nope": w.d_nope, "d_v": w.d_v, "cache_dtype": w.latent_dtype,
+            "layout": w.layout, "block_size": w.block_size, "num_parts": num_parts,
+            "l2": l2_note,
+            "parallelism": "independent replica per GPU (batch-parallel, no collective)"}
+
+
 # ----------------------------------------------------------------------------
 # CPU baseline (the float64 oracle)
 # ----------------------------------------------------------------------------
-
-def oracle_sample(w, budget_s: float, start_b: int = 0):
-    """Time the oracle on whole sequences (all heads) until about budget_s has
-    elapsed; return (attributed cache bytes, seconds, sequences, cores)."""
-    import numpy as np
-
-    import mla_inputs as mi
-    import oracle as O
-    inp = O.workload_inputs_f64(w)
-    per_tok = O.mla_cache_bytes_per_token(w.latent_dtype, w.dtype, w.d_c, w.d_r, w.block_size)
-    total_t, total_bytes, nseq = 0.0, 0.0, 0
-    b = start_b
-    while total_t < budget_s and nseq < w.B:
-        L = int(inp["lens"][b])
-        seqs = [O.sequence_view(w, b, L)]
-        t0 = time.perf_counter()
-        O.decode_reference(inp["q_nope"][[b]], inp["q_rope"][[b]], inp["q_pos"][[b]],
-                           inp["w_uk"], inp["w_uv"], seqs)
-        total_t += time.perf_counter() - t0
-        total_bytes += L * per_tok
-        nseq += 1
-        b = (b + 1) % w.B
-    return total_bytes, total_t, nseq, blas_threads()
-
 
 def blas_threads() -> int:
     try:
@@ -221,17 +248,57 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def oracle_sample(w, budget_s: float, start: int = 0):
+    """Time the oracle (the non-absorbed definition) on windows of heads of
+    whole sequences until about budget_s has elapsed.  Returns (attributed
+    cache bytes, seconds, description, cores); each window is charged its
+    share H/h of the sequence's cache bytes."""
+    import oracle as O
+    inp = O.workload_inputs_f64(w)
+    per_tok = O.mla_cache_bytes_per_token(w.latent_dtype, w.dtype, w.d_c, w.d_r, w.block_size)
+    seq_cache = {}
+
+    def seq(b):
+        if b not in seq_cache:
+            seq_cache.clear()
+            seq_cache[b] = O.sequence_view(w, b, int(inp["lens"][b]))
+        return seq_cache[b]
+
+    def run(b, heads):
+        s = seq(b)
+        t0 = time.perf_counter()
+        O.decode_reference(inp["q_nope"][[b]], inp["q_rope"][[b]], inp["q_pos"][[b]],
+                           inp["w_uk"], inp["w_uv"], [s], heads=heads)
+        return time.perf_counter() - t0
+
+    # heads per window: the whole head set unless one head already takes a
+    # sizeable share of the budget
+    t1 = run(start % w.B, [0])
+    H = int(max(1, min(w.h, (budget_s / 4) // max(t1, 1e-6))))
+    total_t, total_bytes, windows = 0.0, 0.0, 0
+    i = 0
+    while total_t < budget_s and windows < 4 * w.B:
+        b = (start + i) % w.B
+        h0 = (i * H) % w.h
+        heads = [(h0 + k) % w.h for k in range(H)]
+        total_t += run(b, heads)
+        total_bytes += int(inp["lens"][b]) * per_tok * H / w.h
+        windows += 1
+        i += 1
+    desc = (f"{windows} window(s) of {H} of {w.h} heads of whole sequences of the workload, "
+            f"cache bytes attributed pro rata (H/h of each sequence's cache), float64 numpy, "
+            f"{total_t:.1f} s")
+    return total_bytes, total_t, desc, blas_threads()
+
+
 def run_reference(args) -> None:
     """--impl reference: the float64 oracle on the host cores, K timed steps of a
     bounded sample each (a window of heads of one sequence per step)."""
-    import numpy as np
-
-    import mla_inputs as mi
     import oracle as O
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = mi.workload(WORKLOAD)
+    w = resolve_workload(args.workload)
     inp = O.workload_inputs_f64(w)
     per_tok = O.mla_cache_bytes_per_token(w.latent_dtype, w.dtype, w.d_c, w.d_r, w.block_size)
     seq_cache = {}
@@ -243,9 +310,10 @@ def run_reference(args) -> None:
         return seq_cache[b]
 
     def one(b, heads):
+        s = seq(b)
         t0 = time.perf_counter()
         O.decode_reference(inp["q_nope"][[b]], inp["q_rope"][[b]], inp["q_pos"][[b]],
-                           inp["w_uk"], inp["w_uv"], [seq(b)], heads=heads)
+                           inp["w_uk"], inp["w_uv"], [s], heads=heads)
         return time.perf_counter() - t0
 
     # calibrate: seconds per head, then heads per step so that the run takes ~2 minutes
@@ -263,27 +331,19 @@ def run_reference(args) -> None:
             total_t += dt
             total_bytes += int(inp["lens"][b]) * per_tok * H / w.h
     value = total_bytes / total_t / 1e9
-    sample = (f"{H} of {w.h} heads of one sequence (L={w.L}) per step, cache bytes attributed "
+    sample = (f"{H} of {w.h} heads of one sequence per step, cache bytes attributed "
               f"pro rata (H/h of the sequence's cache)")
     cores = blas_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": bench_config(w, None),
+        "data": "synthetic", "config": bench_config(w, None, "host run: no GPU cache involved"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
-
-
-def bench_config(w, num_parts) -> dict:
-    return {"workload": w.name, "B": w.B, "h": w.h, "L": w.L, "d_c": w.d_c, "d_r": w.d_r,
-            "d_nope": w.d_nope, "d_v": w.d_v, "cache_dtype": w.latent_dtype,
-            "block_size": w.block_size, "num_parts": num_parts,
-            "l2": "inputs larger than L2 (604 MB latent cache per step)",
-            "parallelism": "independent replica per GPU (batch-parallel, no collective)"}
 
 
 # ----------------------------------------------------------------------------
@@ -294,7 +354,6 @@ def run_ours(args) -> None:
     import torch
     import torch.distributed as dist
 
-    import mla_inputs as mi
     from mla_latent_kv_72_b300 import binding as C
     from mla_latent_kv_72_b300 import build as mbuild
     from mla_latent_kv_72_b300.workload import DeviceWorkload
@@ -307,45 +366,63 @@ def run_ours(args) -> None:
         mbuild.build()
     barrier()
     C.lib()
-    w = mi.workload(WORKLOAD)
+    w = resolve_workload(args.workload)
     dw = DeviceWorkload(w, device=f"cuda:{local}", num_parts=args.parts)
     stream = torch.cuda.current_stream()
 
-    # warm-up
-    for _ in range(args.warmup):
-        dw.step()
-    torch.cuda.synchronize()
-    if dw.check_status() != 0:
-        raise RuntimeError(f"device status {dw.check_status()} after warm-up")
+    # inputs of one step smaller than L2 are flushed from it between timed
+    # steps (outside the per-step events); larger ones stream through it
+    per_step_in = dw.cache_bytes()
+    flush = per_step_in < 2 * L2_BYTES
+    scrub = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dw.device) \
+        if flush else None
+    l2_note = (f"L2 flushed between timed steps by writing {2 * L2_BYTES >> 20} MiB "
+               f"(outside the per-step events)" if flush else
+               f"inputs larger than L2 ({per_step_in / 1e6:.0f} MB of latent cache per step)")
 
-    # timed region: K steps, events around every decode launch for the roofline
-    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    n_st = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_st)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        # settle: untimed steps until the clocks sit at their loaded state
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < args.settle_s:
+            for _ in range(8):
+                dw.step()
+            torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            dw.step()
+        torch.cuda.synchronize()
+        if dw.check_status() != 0:
+            raise RuntimeError(f"device status {dw.check_status()} after warm-up")
         barrier()
         torch.cuda.synchronize()
         start.record(stream)
-        for i in range(args.steps):
+        for i in range(n_st):
+            if flush:
+                scrub.fill_(float(i))
+            ev[i][0].record(stream)
             dw.absorb()
-            ev_s[i].record(stream)
+            ev[i][1].record(stream)
             dw.attend()
-            ev_e[i].record(stream)
+            ev[i][2].record(stream)
             dw.combine()
             dw.project()
+            ev[i][3].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
         barrier()
     clocks = clk.result()
-    total_s = start.elapsed_time(end) / 1e3
-    decode_s = sum(a.elapsed_time(b) for a, b in zip(ev_s, ev_e)) / 1e3 / args.steps
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_s = (sum(step_ms) if flush else start.elapsed_time(end)) / 1e3
     max_total = reduce_max(total_s)
     assert dw.check_status() == 0
 
     step_bytes = dw.step_bytes()
     step_flops = dw.step_flops()
-    value = aggregate(step_bytes * args.steps, world, max_total) / 1e9
-    tflops = aggregate(step_flops * args.steps, world, max_total) / 1e12
+    value = aggregate(step_bytes * n_st, world, max_total) / 1e9
+    tflops = aggregate(step_flops * n_st, world, max_total) / 1e12
 
     # end to end through the C ABI: pinned host inputs in, output back, every step
     h_qn = dw.q_nope.cpu().pin_memory()
@@ -355,7 +432,7 @@ def run_ours(args) -> None:
     h2d = h_qn.numel() * h_qn.element_size() + h_qr.numel() * h_qr.element_size() + \
         h_pos.numel() * h_pos.element_size()
     d2h = h_out.numel() * h_out.element_size()
-    e2e_steps = max(3, min(args.steps, 200))
+    e2e_steps = max(3, min(n_st, 200))
 
     def e2e_step():
         dw.q_nope.copy_(h_qn, non_blocking=True)
@@ -381,35 +458,47 @@ def run_ours(args) -> None:
         return
     peaks, peak_kind = load_peaks()
     hbm = float(peaks.get("hbm_gbs", PEAK_FALLBACK["hbm_gbs"]))
-    tc = float(peaks.get("bf16_tflops_sustained", PEAK_FALLBACK["bf16_tflops_sustained"]))
-    dec_bytes = dw.cache_bytes() + w.B * w.h * (w.d_c + w.d_r) * 2 + dw.table_np.size * 4 + w.B * 4
-    dec_flops = float(dw.lens_np.sum()) * w.h * 2 * (w.d_c + w.d_r + w.d_c)
-    achieved = dec_bytes / decode_s / 1e9
+    tc_burst = float(peaks.get("bf16_tflops", PEAK_FALLBACK["bf16_tflops"]))
+    tc_sust = float(peaks.get("bf16_tflops_sustained", PEAK_FALLBACK["bf16_tflops_sustained"]))
+    dec_bytes, dec_flops = dw.decode_bytes(), dw.decode_flops()
+    dstat = step_stats(dec_ms)
+    dec_s = dstat["mean_ms"] / 1e3
+    roof = roofline(dec_bytes, dec_flops, dec_s, hbm, tc_burst)
     sha = kernel_source_sha()
-    traffic = read_profile_traffic(sha)
+    roof.update({
+        "traffic": read_profile_traffic(w.name, sha),
+        "kernel": "mla_decode_fwd", "kernel_source_sha256": sha,
+        "peak_source": f"{peak_kind} MEASURED_PEAKS.json (hbm_gbs; bf16_tflops burst)",
+        "alg_bytes": dec_bytes, "alg_flops": dec_flops,
+        "decode_ms": dstat["mean_ms"], "decode_median_ms": dstat["median_ms"],
+        "decode_min_ms": dstat["min_ms"],
+        "frac_at_median": roofline(dec_bytes, dec_flops, dstat["median_ms"] / 1e3, hbm,
+                                   tc_burst)["frac"],
+        "hbm_frac": dec_bytes / dec_s / 1e9 / hbm,
+        "tensor_frac_burst": dec_flops / dec_s / 1e12 / tc_burst,
+        "tensor_frac_sustained": dec_flops / dec_s / 1e12 / tc_sust,
+    })
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        nbytes, secs, nseq, cores = oracle_sample(w, args.cpu_budget)
+        nbytes, secs, desc, cores = oracle_sample(w, args.cpu_budget)
         cpu = {"value": nbytes / secs / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{nseq} whole sequence(s) of the workload (L={w.L}, all {w.h} heads), "
-                         f"float64 numpy, {secs:.1f} s"}
+               "sample": desc}
+    sstat = step_stats(step_ms)
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * max_total / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": bench_config(w, dw.num_parts),
-        "tflops": tflops, "steps_per_s": args.steps / max_total,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic,
-                     "kernel": "mla_decode_fwd", "peak_source": f"{peak_kind} hbm_gbs",
-                     "decode_ms": decode_s * 1e3,
-                     "tensor_frac": dec_flops / decode_s / 1e12 / tc,
-                     "tensor_peak_tflops": tc},
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n_st,
+        "warmup": args.warmup, "ms_per_step": 1e3 * max_total / n_st,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic", "config": bench_config(w, dw.num_parts, l2_note),
+        "tflops": tflops, "steps_per_s": n_st / max_total,
+        "step_ms": sstat,
+        "roofline": roof,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 4 * n_st,
         "clocks": clocks,
+        "settle_s": args.settle_s,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -418,11 +507,15 @@ def run_ours(args) -> None:
 def main(argv=None) -> None:
     p = argparse.ArgumentParser(description=__doc__)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=None,
+                   help="workload index 1..5 or name (default: the V3-shaped workload, 3)")
     p.add_argument("--parts", type=int, default=None,
                    help="balanced parts of the block stream (default: half the SM count)")
+    p.add_argument("--settle-s", type=float, default=0.5,
+                   help="seconds of untimed steps before the warm-up")
     p.add_argument("--cpu-budget", type=float, default=15.0,
                    help="seconds of oracle work for the CPU baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -72,9 +72,17 @@ typedef enum {
 #define MLA_DEV_BAD_LENGTH 2     /* seq_len > max_blocks_per_seq * block_size */
 #define MLA_DEV_WAIT_TIMEOUT 3   /* a bounded pipeline wait gave up */
 
-/* Flags of mla_decode_fwd. */
+/* Flags of mla_decode_fwd (exactly one of them). */
 #define MLA_DECODE_AUTO 0u          /* tensor-core kernel where supported, else SIMT */
 #define MLA_DECODE_FORCE_SIMT 1u    /* always the CUDA-core (SIMT) kernel */
+/* Diagnostic, for testing the device-side error path: the tensor-core
+ * kernel's MMA issuer first waits on a barrier that nothing signals, with a
+ * limit of about 1e4 SM clocks.  The wait runs out, the kernel writes
+ * MLA_DEV_WAIT_TIMEOUT to *dev_status, every other role of the kernel sees
+ * the abort and winds down (in-flight copies are waited for, tensor memory
+ * is freed) and the kernel returns; the outputs are left unwritten.  Calls
+ * that would run the SIMT kernel return MLA_ERR_ARG with this flag. */
+#define MLA_DECODE_TEST_WAIT_TIMEOUT 2u
 
 /*
  * Paged latent cache (iotdigitaltwinplm.com "Interaction with quantisation
@@ -186,7 +194,7 @@ int mla_decode_num_partials(int B, int num_parts);
  *   o_part     [mla_decode_num_partials(B, num_parts), h, d_c] float32 (output)
  *   lse_part   [mla_decode_num_partials(B, num_parts), h] float32 (output)
  *   dev_status int32 device word, may be NULL (see conventions)
- *   flags      MLA_DECODE_AUTO or MLA_DECODE_FORCE_SIMT
+ *   flags      MLA_DECODE_AUTO, MLA_DECODE_FORCE_SIMT or MLA_DECODE_TEST_WAIT_TIMEOUT
  * Supported dtypes: (q, latent, rope) = (F32, F32, F32) on the SIMT kernel;
  * (BF16, BF16, BF16) and (BF16, FP8E4M3, BF16) on both kernels.  The tensor-core
  * kernel runs for d_c = 512, d_r = 64, block_size = 64, h <= 128; for an FP8
@@ -233,7 +241,9 @@ int mla_combine(const float* o_part, const float* lse_part, const int32_t* seq_l
  * (the array holds 68 MiB on every device that loads the library, until the
  * process exits); larger calls return MLA_ERR_SHAPE and launch nothing.
  * The first call on a device looks up the array's device address with that
- * device current; make it before any stream capture.  All calls share the
+ * device current; make it before any stream capture.  The address is kept per
+ * device and CUDA context, so a call after a device reset looks it up again
+ * (that call, too, belongs outside a stream capture).  All calls share the
  * array: calls that overlap on the GPU race on it.  Nothing in it needs to
  * start at zero (each call writes every slot it reads).  Allocates nothing.
  */

@@ -17,6 +17,12 @@ MLA_FP8E4M3 = 2
 
 MLA_DECODE_AUTO = 0
 MLA_DECODE_FORCE_SIMT = 1
+MLA_DECODE_TEST_WAIT_TIMEOUT = 2
+
+MLA_DEV_OK = 0
+MLA_DEV_BAD_BLOCK = 1
+MLA_DEV_BAD_LENGTH = 2
+MLA_DEV_WAIT_TIMEOUT = 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None

@@ -53,7 +53,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     objs = []
     for s in SOURCES:
         obj = os.path.join(objdir, s.replace(".cu", ".o"))
-        cmd = [nvcc(), *ARCH, *FLAGS, "-I", INCLUDE, "-dc" if False else "-c",
+        cmd = [nvcc(), *ARCH, *FLAGS, "-I", INCLUDE, "-c",
                os.path.join(CSRC, s), "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]

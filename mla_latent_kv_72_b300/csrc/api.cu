@@ -96,7 +96,9 @@ int mla_decode_fwd(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
                    float* lse_part, int32_t* dev_status, unsigned flags, void* stream) {
   if (!q_cat || !block_table || !seq_lens || !o_part || !lse_part) return MLA_ERR_ARG;
   if (B <= 0 || h <= 0 || num_parts <= 0 || max_blocks_per_seq <= 0) return MLA_ERR_ARG;
-  if (flags > MLA_DECODE_FORCE_SIMT) return MLA_ERR_ARG;
+  if (flags != MLA_DECODE_AUTO && flags != MLA_DECODE_FORCE_SIMT &&
+      flags != MLA_DECODE_TEST_WAIT_TIMEOUT)
+    return MLA_ERR_ARG;
   int st = check_cache(kv);
   if (st != MLA_OK) return st;
   if (!is_float_dtype(q_dtype)) return MLA_ERR_DTYPE;
@@ -106,10 +108,13 @@ int mla_decode_fwd(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
   if (!aligned16(q_cat) || !aligned16(o_part)) return MLA_ERR_ALIGN;
   float scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / sqrt(128.0 + kv->d_r));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (flags != MLA_DECODE_FORCE_SIMT && mla::decode_tc_supported(q_dtype, *kv, h)) {
+  const bool tc = flags != MLA_DECODE_FORCE_SIMT && mla::decode_tc_supported(q_dtype, *kv, h);
+  // the diagnostic timeout exists only in the pipelined tensor-core kernel
+  if (flags == MLA_DECODE_TEST_WAIT_TIMEOUT && !tc) return MLA_ERR_ARG;
+  if (tc) {
     return from_cuda(mla::launch_decode_tc(q_cat, *kv, block_table, max_blocks_per_seq, seq_lens,
                                            B, h, num_parts, scale, o_part, lse_part, dev_status,
-                                           s));
+                                           flags == MLA_DECODE_TEST_WAIT_TIMEOUT, s));
   }
   return from_cuda(mla::launch_decode_simt(q_cat, q_dtype, *kv, block_table, max_blocks_per_seq,
                                            seq_lens, B, h, num_parts, scale, o_part, lse_part,

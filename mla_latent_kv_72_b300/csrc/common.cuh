@@ -169,7 +169,7 @@ cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, i
 cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                              int B, int h, int num_parts, float scale, float* o_part,
-                             float* lse_part, int32_t* status, cudaStream_t s);
+                             float* lse_part, int32_t* status, bool test_timeout, cudaStream_t s);
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* seq_lens,
                            int block_size, int max_blocks, int B, int h, int d_c, int num_parts,

@@ -12,37 +12,55 @@
 //
 // Work split.  One float32 accumulator for 128 heads x 512 latent columns
 // fills the whole 512-column tensor memory of an SM, so a pair of CTAs (a
-// cluster of 2) shares each piece of work:
-//   CTA r owns output columns [256 r, 256 r + 256) of the latent (O_r in TMEM)
-//   and the matching slice of the 576-d score contraction: CTA 0 the latent
-//   columns 0..255 plus the 64 RoPE columns, CTA 1 the latent columns 256..511.
-//   Each CTA TMA-loads exactly its own columns of every cache block (the pair
-//   reads each byte of the cache once), computes its partial score tile, and
-//   writes it into the peer's shared memory (one release-ordered remote
-//   arrive per warp); both CTAs then hold the same S = S_0 + S_1 (float addition
-//   commutes, so both run a bit-identical online softmax) and write the same
-//   P, which each multiplies into its own O_r.
+// cluster of 2) shares each piece of work.  CTA r owns latent output columns
+// [256 r, 256 r + 256) (O_r in TMEM) and the matching slice of the 576-d
+// score contraction: latent columns [256 r, 256 r + 256) plus RoPE dims
+// [32 r, 32 r + 32).  Each CTA TMA-loads exactly its own columns of every
+// cache block (four 64x64 latent boxes, 128-byte swizzle, and one 32x64 RoPE
+// box, 64-byte swizzle), so the pair reads each byte of the cache once.  Its
+// partial score tile (128 heads x 64 tokens) goes to the peer through
+// distributed shared memory: both CTAs keep the top 24 bits of every partial
+// (their own and the peer's) and use the freed low byte of each value sent
+// as a per-use tag, which the receiver polls for; both then hold the same
+// S = S_0 + S_1 (the addition commutes), run a bit-identical online softmax
+// and write the same P, which each multiplies into its own O_r.
 //
 // Schedule.  The grid is persistent: pair p runs part p of the balanced
 // partition of the whole block stream (all sequences' blocks in order, see
 // common.cuh), one segment (the part's blocks of one sequence) after another,
 // and writes one partial (o, lse) per segment into slot p + b.
 //
-// Roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
-// tcgen05.mma (one lane), warps 2..5 and 6..9 are two softmax warpgroups that
-// take alternate tiles (ping-pong), so that the exchange and softmax of one
-// tile overlap those of the next.  The running maximum is handed from one
-// group to the other per tile; O is rescaled only when the maximum grows by
-// more than kTau (log2 units), so P <= 2^kTau in bf16.
+// Roles of the bf16 variant (19 warps, 608 threads):
+//   warp 0       TMA producer: a ring of 4 stages (36 KB each) plus an L2
+//                prefetch of the tile one ahead of the load;
+//   warp 1       score MMA issuer: S = Q K^T, 16 TS steps (query latent slice
+//                in TMEM) + 2 SS steps (query RoPE slice in shared memory),
+//                M = 128 heads, N = 64 tokens;
+//   warps 2..17  two softmax groups of 8 warps, tile k to group k % 2; two
+//                warps per TMEM lane quarter split a row's 64 scores (32
+//                each) and meet on a 64-thread named barrier for the row max;
+//   warp 18      P.C MMA issuer: O_r += P C_r, 4 TS steps (P in TMEM, the
+//                latent boxes as an MN-major B operand), N = 256.
+// The FP8-latent variant has 3 bf16 stages, 2 e4m3 landing buffers, two
+// converter warps (e4m3 x block scale -> bf16 into the swizzled stage) and a
+// single event-driven MMA warp for both kinds of MMA.
 //
-// TMEM columns: O_r [0, 256), S [256, 320), Q_r [320, 320 + 160) as the MMA
-// A operand (bf16 pairs).  Every wait is bounded; on a timeout the kernel
-// writes MLA_DEV_WAIT_TIMEOUT to the status word and winds down.
+// The running maximum is handed from one group to the other per tile; O is
+// rescaled only when the maximum grows by more than kTau (log2 units), so
+// P <= 2^kTau in bf16.
+//
+// TMEM columns: O_r [0, 256), S [256, 320), query latent slice [320, 448)
+// (bf16 pairs, the A operand of the score MMA), P x 2 [448, 512) (bf16
+// pairs, the A operand of the P.C MMA).  Every wait is bounded; on a timeout
+// the kernel writes MLA_DEV_WAIT_TIMEOUT to the status word and winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
+#include "device_registry.h"
 #include "tc_ptx.cuh"
 
 namespace mla {
@@ -136,7 +154,8 @@ enum {
   BAR_SEG = BAR_O_FREE + 1,             // softmax (all warps): end-of-segment rendezvous
   BAR_DRAIN = BAR_SEG + 1,
   BAR_DRAIN_O = BAR_DRAIN + 1,          // bf16 variant: the P.C issuer's own drain
-  BAR_COUNT = BAR_DRAIN_O + 1,
+  BAR_NEVER = BAR_DRAIN_O + 1,          // signalled by nothing (diagnostic timeout wait)
+  BAR_COUNT = BAR_NEVER + 1,
 };
 static_assert(BAR_COUNT <= kNumBars, "barrier array");
 
@@ -151,6 +170,9 @@ struct TcParams {
   int max_blocks, B, h, num_parts, num_blocks;
   float scale_log2;
   long long wait_limit;
+  // diagnostic: the MMA issuer's first wait is made on BAR_NEVER with this
+  // limit (SM clocks), so that the kernel takes its timeout path; 0 = off
+  long long test_wait_limit;
 };
 
 // 2^x on the SFU (subnormal results flush to zero: P values that small do not
@@ -334,6 +356,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     mbar_init(bar(BAR_SEG), kSoftWarps);
     mbar_init(bar(BAR_DRAIN), 1);
     mbar_init(bar(BAR_DRAIN_O), 1);
+    mbar_init(bar(BAR_NEVER), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -515,7 +538,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     its.init(p.seq_lens, p.max_blocks, b_first, blk_first);
     int seg_s = 0;
     bool ok = true;
-    for (int ks = 0; ks < ntiles; ++ks) {
+    if (p.test_wait_limit > 0) {
+      // diagnostic: a wait that nothing ends, with a short limit
+      bool fin = true;
+      if (lane == 0)
+        fin = mbar_spin_or_abort(bar(BAR_NEVER), 0, p.test_wait_limit, abort_flag, &timed_out);
+      if (!__shfl_sync(0xffffffffu, fin ? 1 : 0, 0)) ok = false;
+    }
+    for (int ks = 0; ok && ks < ntiles; ++ks) {
       const int st = ks % kStages;
       const bool first = (ks == 0) || (its.blk == 0);
       const bool last = (ks == ntiles - 1) || (its.blk == its.nb - 1);
@@ -625,6 +655,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     int nv_s = its.valid();  // valid tokens of tile ks
     long long idle_since = clock64();
     bool ok = true;
+    if (p.test_wait_limit > 0) {
+      // diagnostic: a wait that nothing ends, with a short limit
+      bool fin = true;
+      if (lane == 0)
+        fin = mbar_spin_or_abort(bar(BAR_NEVER), 0, p.test_wait_limit, abort_flag, &timed_out);
+      if (!__shfl_sync(0xffffffffu, fin ? 1 : 0, 0)) ok = false;
+    }
     // lane 0: issue O(ko) if its P is ready (state is advanced by advance_o on all lanes)
     auto try_issue_o_lane0 = [&]() -> bool {
       if (ko >= ks) return false;
@@ -652,7 +689,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       if (ko + 1 < ntiles) ito.next();
       ++ko;
     };
-    while (ko < ntiles) {
+    while (ok && ko < ntiles) {
       bool did = false;
       // O(ko) first: it frees a P buffer and a stage
       {
@@ -1206,17 +1243,24 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
   return r == CUDA_SUCCESS;
 }
 
+// compute capability major of the current device (0 if there is none)
 int device_major() {
-  static int major = -1;
-  if (major < 0) {
-    int dev = 0;
-    cudaDeviceProp prop;
-    if (cudaGetDevice(&dev) == cudaSuccess && cudaGetDeviceProperties(&prop, dev) == cudaSuccess)
-      major = prop.major;
-    else
-      major = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
   }
-  return major;
+  return device_registry().value(
+      dev,
+      [dev]() {
+        int major = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) {
+          cudaGetLastError();
+          major = 0;
+        }
+        return major;
+      },
+      0);
 }
 
 }  // namespace
@@ -1227,18 +1271,26 @@ extern "C" int mla_debug_set_trace(void* p) {
 }
 #endif
 
+DeviceRegistry& device_registry() {
+  static DeviceRegistry reg;
+  return reg;
+}
+
+// The driver's tensor-map encoder (one entry point for every device of the
+// process), looked up once.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static std::once_flag flag;
+  std::call_once(flag, []() {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+    else
+      cudaGetLastError();
+  });
   return fn;
 }
 
@@ -1270,14 +1322,16 @@ template <bool kFp8>
 cudaError_t launch_variant(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope,
                            const CUtensorMap& tm_q, const TcParams& prm, int num_parts,
                            cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<kFp8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<kFp8>::kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // the dynamic shared-memory limit is a per-device setting: once per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int r = device_registry().once(dev, kFp8 ? kSetupDecodeFp8 : kSetupDecodeBf16, []() {
+    return (int)cudaFuncSetAttribute(decode_tc_kernel<kFp8>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg<kFp8>::kSmemAlloc);
+  });
+  if (r != 0) return r < 0 ? cudaErrorInvalidDevice : (cudaError_t)r;
   dim3 grid(2 * num_parts);
   decode_tc_kernel<kFp8><<<grid, Cfg<kFp8>::kThreads, Cfg<kFp8>::kSmemAlloc, s>>>(tm_lat, tm_rope,
                                                                                  tm_q, prm);
@@ -1289,7 +1343,8 @@ cudaError_t launch_variant(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope
 cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                              int B, int h, int num_parts, float scale, float* o_part,
-                             float* lse_part, int32_t* status, cudaStream_t s) {
+                             float* lse_part, int32_t* status, bool test_timeout,
+                             cudaStream_t s) {
   const bool fp8 = kv.latent_dtype == MLA_FP8E4M3;
   CUtensorMap tm_lat, tm_rope, tm_q;
   const uint64_t rows = (uint64_t)kv.num_blocks * kv.block_size;
@@ -1314,6 +1369,7 @@ cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
   prm.num_blocks = kv.num_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.wait_limit = 4000000000LL;  // about 2 s of SM clock
+  prm.test_wait_limit = test_timeout ? 20000 : 0;  // about 10 us
   return fp8 ? launch_variant<true>(tm_lat, tm_rope, tm_q, prm, num_parts, s)
              : launch_variant<false>(tm_lat, tm_rope, tm_q, prm, num_parts, s);
 }

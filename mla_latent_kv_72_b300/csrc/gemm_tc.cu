@@ -22,6 +22,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "device_registry.h"
 #include "tc_ptx.cuh"
 
 namespace mla {
@@ -252,15 +253,17 @@ int n_tile_for(int B, int cap = kMaxN) {
   return (n + 15) / 16 * 16;
 }
 
+// the dynamic shared-memory limit is a per-device setting: once per device
 template <bool kMN>
 cudaError_t set_smem_attr() {
-  static bool done = false;
-  if (!done) {
-    cudaError_t e = cudaFuncSetAttribute(head_gemm_kernel<kMN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemMax);
-    if (e != cudaSuccess) return e;
-    done = true;
-  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int r = device_registry().once(dev, kMN ? kSetupGemmMN : kSetupGemmK, []() {
+    return (int)cudaFuncSetAttribute(head_gemm_kernel<kMN>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmemMax);
+  });
+  if (r != 0) return r < 0 ? cudaErrorInvalidDevice : (cudaError_t)r;
   return cudaSuccess;
 }
 

@@ -17,35 +17,71 @@
 // decode of the same call first.  Host code cannot use the array's name as a
 // device address, so the first call on each device looks the address up with
 // cudaGetSymbolAddress while that device is current; make that first call
-// before any stream capture.
+// before any stream capture.  The address is kept per device together with
+// the unique id of the CUDA context it was looked up in: after a device reset
+// (a new primary context, where the module and the array may sit elsewhere)
+// the next call looks it up again.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
+#include "device_registry.h"
 
 namespace mla {
 namespace {
 
 constexpr size_t kScratchPartFloats = size_t(16) << 20;  // o_part: slots * h * d_c
 constexpr size_t kScratchLseFloats = size_t(1) << 20;    // lse_part: slots * h
-constexpr int kMaxDevices = 64;
-
 static __device__ __align__(256) float g_scratch[kScratchPartFloats + kScratchLseFloats];
 
 std::mutex g_mu;
 float* g_addr[kMaxDevices] = {nullptr};
+unsigned long long g_ctx_id[kMaxDevices] = {0};
 
-// Device address of g_scratch on the current device (looked up once per device).
+// Unique id of the calling thread's current CUDA context (0 if none can be had).
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag flag;
+  std::call_once(flag, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    cudaGetLastError();
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+      get_id(ctx, &id) == CUDA_SUCCESS)
+    return id;
+  return 0;
+}
+
+// Device address of g_scratch on the current device, looked up once per
+// (device, context).
 cudaError_t scratch_address(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_addr[dev] == nullptr) {
+  if (g_addr[dev] == nullptr || ctx == 0 || g_ctx_id[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess) return e;
     g_addr[dev] = static_cast<float*>(p);
+    // the look-up makes the runtime's primary context current if this thread
+    // had none, so the id is read again after it
+    g_ctx_id[dev] = current_context_id();
   }
   *out = g_addr[dev];
   return cudaSuccess;

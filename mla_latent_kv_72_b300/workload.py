@@ -148,6 +148,19 @@ class DeviceWorkload:
         out = B * h * w.d_v * self.out.element_size()
         return self.cache_bytes() + q_in + wts + table + out
 
+    def decode_bytes(self) -> float:
+        """Algorithmic bytes of one mla_decode_fwd launch: every cached token
+        once, the absorbed queries, the block table and the lengths."""
+        w = self.w
+        el = 4 if w.dtype == "f32" else 2
+        return (self.cache_bytes() + w.B * w.h * (w.d_c + w.d_r) * el
+                + self.table_np.size * 4 + w.B * 4)
+
+    def decode_flops(self) -> float:
+        """2 * h * (d_c + d_r) score flops plus 2 * h * d_c P.C flops per cached token."""
+        w = self.w
+        return float(self.lens_np.sum()) * w.h * 2 * (w.d_c + w.d_r + w.d_c)
+
     def step_flops(self) -> float:
         """2 * h * (d_c + d_r + d_c) per cached token, plus the two per-head GEMMs."""
         w = self.w

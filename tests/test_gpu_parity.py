@@ -1,8 +1,10 @@
 """GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
 
-Tolerance (stated by the task's target): max|err| / max|ref| <= 1e-4 for the
-float32 workload and <= 2e-2 for bf16 / FP8 workloads, on the output after
-W_UV and on the latent output; paged gathers are bit-exact.
+Tolerance: max|err| / max|ref| <= 1e-4 for the float32 workload and <= 2e-2
+for bf16 / FP8 workloads, on the output after W_UV and on the latent output.
+The log-sum-exp is compared with an absolute bound of the same size: an
+error d in lse is a relative error of about d in the softmax denominator.
+Paged gathers are bit-exact.
 """
 import numpy as np
 import pytest
@@ -44,19 +46,28 @@ def make(w, **kw):
     return DeviceWorkload(w, **kw)
 
 
-def compare(w, dw, batch, heads, tol):
-    ref = oracle_for(w, batch, heads)
-    hs = list(range(w.h)) if heads is None else list(heads)
+def abs_err(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.all(np.isfinite(got)), "non-finite values in the GPU result"
+    return float(np.abs(got - np.asarray(ref, dtype=np.float64)).max())
+
+
+def check_against(ref, dw, batch, heads, tol):
+    hs = list(range(dw.w.h)) if heads is None else list(heads)
     out = dw.out.float().cpu().numpy()[np.ix_(list(batch), hs)]
     o_lat = dw.o_lat.float().cpu().numpy()[np.ix_(list(batch), hs)]
     lse = dw.lse.float().cpu().numpy()[np.ix_(list(batch), hs)]
     e_out = rel_err(out, ref["out"])
     e_lat = rel_err(o_lat, ref["o_lat"])
-    e_lse = rel_err(lse, ref["lse"])
+    e_lse = abs_err(lse, ref["lse"])
     assert e_out <= tol, ("out", e_out)
     assert e_lat <= tol, ("o_lat", e_lat)
     assert e_lse <= tol, ("lse", e_lse)
     return e_out, e_lat, e_lse
+
+
+def compare(w, dw, batch, heads, tol):
+    return check_against(oracle_for(w, batch, heads), dw, batch, heads, tol)
 
 
 # ----------------------------------------------------------------------------
@@ -125,6 +136,14 @@ def expected_slots(lens, block_size, num_parts):
     return slots
 
 
+# Two part counts split the key range at different blocks, so the online
+# softmax runs against different running maxima and each P is rounded to bf16
+# relative to a different maximum (up to 2^-9 of each term) before the P.C
+# MMA; the merged latent output is then stored in bf16 (2^-9 of each element).
+# Their difference is bounded by those two roundings: 4e-3 of max|o_lat|.
+PART_TOL = 4e-3
+
+
 @pytest.mark.parametrize("num_parts", [1, 2, 7, 64, 148])
 def test_part_count_invariance(num_parts):
     w = mi.scaled(mi.workload(3), B=2, h=128, L=3000)
@@ -135,8 +154,9 @@ def test_part_count_invariance(num_parts):
     torch.cuda.synchronize()
     ref = dw1.o_lat.float().cpu().numpy()
     o = dw.o_lat.float().cpu().numpy()
-    assert np.abs(o - ref).max() / np.abs(ref).max() < 1e-2
-    compare(w, dw, range(w.B), [0, 77, 127], TOL["bf16"])
+    assert np.abs(o - ref).max() / np.abs(ref).max() < PART_TOL
+    assert abs_err(dw.lse.cpu().numpy(), dw1.lse.cpu().numpy()) < PART_TOL
+    compare(w, dw, range(w.B), None, TOL["bf16"])
 
 
 @pytest.mark.parametrize("flags", [0, 1], ids=["auto", "simt"])
@@ -260,22 +280,127 @@ def test_out_proj_matches_oracle():
 
 
 # ----------------------------------------------------------------------------
-# full-size workloads: sampled outputs, computed one by one by the oracle
+# full-size workloads, in the launch configuration the benchmark times
 # ----------------------------------------------------------------------------
+#
+# The checker is the oracle's absorbed form (decode_absorbed), which the CPU
+# pins tie to the non-absorbed definition at 1e-12; it is cheap enough to
+# check every (sequence, head) output of the full workloads.
 
-SAMPLES = {2: [(0, 0), (31, 7), (63, 15)],
-           3: [(0, 0), (17, 64), (63, 127)],
-           4: [(0, 3), (64, 100), (127, 127)],
-           5: [(0, 0), (3, 127)]}
+def absorbed_oracle(w, batch, heads=None):
+    inp = O.workload_inputs_f64(w)
+    seqs = [O.sequence_view(w, b, int(inp["lens"][b])) for b in batch]
+    idx = list(batch)
+    return O.decode_absorbed(inp["q_nope"][idx], inp["q_rope"][idx], inp["q_pos"][idx],
+                             inp["w_uk"], inp["w_uv"], seqs, heads=heads)
 
 
-@pytest.mark.parametrize("idx", [2, 3, 4, 5])
-def test_full_size_sampled(idx):
+def check_full(w, dw, heads=None, chunk=8):
+    for b0 in range(0, w.B, chunk):
+        batch = range(b0, min(w.B, b0 + chunk))
+        check_against(absorbed_oracle(w, batch, heads), dw, batch, heads, TOL["bf16"])
+
+
+# (workload, heads checked, num_parts): every output of workloads 2, 3 and 5;
+# every sequence of workload 4 at 8 heads spread over the 128; workload 5 also
+# with 256 parts, 64 or more key chunks per sequence
+FULL_CASES = {
+    "w2": (2, None, None),
+    "w3": (3, None, None),
+    "w4_8heads": (4, [0, 17, 38, 63, 64, 90, 111, 127], None),
+    "w5": (5, None, None),
+    "w5_256parts": (5, None, 256),
+}
+
+
+@pytest.mark.parametrize("case", list(FULL_CASES))
+def test_full_size_every_output(case):
+    idx, heads, parts = FULL_CASES[case]
     w = mi.workload(idx)
-    dw = make(w)
+    dw = make(w, num_parts=parts)
     dw.step()
     torch.cuda.synchronize()
     assert dw.check_status() == 0
     assert torch.isfinite(dw.out).all()
-    for b, s in SAMPLES[idx]:
-        compare(w, dw, [b], [s], TOL["bf16"])
+    check_full(w, dw, heads)
+
+
+# ----------------------------------------------------------------------------
+# interface conventions and device-side error reporting
+# ----------------------------------------------------------------------------
+
+def test_sixteen_byte_aligned_buffers_give_the_same_bits():
+    # q_cat and o_part 16-byte but not 32-byte aligned: the decode takes its
+    # 16-byte access path, which must give the same bits as the 32-byte one
+    from mla_latent_kv_72_b300 import binding as C
+    w = mi.scaled(mi.workload(3), B=3, L=700)
+    dw = make(w, num_parts=5)
+    dw.absorb()
+    dw.attend()
+    torch.cuda.synchronize()
+    q_big = torch.empty(dw.q_cat.numel() + 16, dtype=dw.q_cat.dtype, device="cuda")
+    q_off = q_big[8:8 + dw.q_cat.numel()].view(dw.q_cat.shape)       # +16 bytes
+    q_off.copy_(dw.q_cat)
+    o_big = torch.empty(dw.o_part.numel() + 8, dtype=torch.float32, device="cuda")
+    o_off = o_big[4:4 + dw.o_part.numel()].view(dw.o_part.shape)     # +16 bytes
+    lse_off = torch.empty_like(dw.lse_part)
+    assert q_off.data_ptr() % 32 == 16 and o_off.data_ptr() % 32 == 16
+    o_off.fill_(float("nan"))
+    C.mla_decode_fwd(q_off, dw.kv, dw.block_table, dw.seq_lens, dw.num_parts, o_off, lse_off,
+                     dev_status=dw.status)
+    torch.cuda.synchronize()
+    assert dw.check_status() == 0
+    slots = sorted(expected_slots(dw.lens_np, w.block_size, dw.num_parts))
+    assert torch.equal(o_off[slots].view(torch.int32), dw.o_part[slots].view(torch.int32))
+    assert torch.equal(lse_off[slots].view(torch.int32), dw.lse_part[slots].view(torch.int32))
+
+
+def test_forced_wait_timeout_is_reported_and_the_device_stays_usable():
+    # MLA_DECODE_TEST_WAIT_TIMEOUT makes the kernel's first MMA wait run on a
+    # barrier that nothing signals, with a short limit: the status word must
+    # read MLA_DEV_WAIT_TIMEOUT and the kernel must return (no hang, no trap)
+    from mla_latent_kv_72_b300 import binding as C
+    for idx in (3, 5):
+        w = mi.scaled(mi.workload(idx), B=2, L=900)
+        dw = make(w, num_parts=3)
+        dw.absorb()
+        torch.cuda.synchronize()
+        C.mla_decode_fwd(dw.q_cat, dw.kv, dw.block_table, dw.seq_lens, dw.num_parts, dw.o_part,
+                         dw.lse_part, dev_status=dw.status, flags=C.MLA_DECODE_TEST_WAIT_TIMEOUT)
+        torch.cuda.synchronize()
+        assert dw.check_status() == C.MLA_DEV_WAIT_TIMEOUT
+        # the context is still good: a normal step afterwards is correct
+        dw.status.zero_()
+        dw.step()
+        torch.cuda.synchronize()
+        assert dw.check_status() == 0
+        compare(w, dw, range(w.B), None, TOL["bf16"])
+    # the SIMT kernel has no pipeline waits: the flag is refused there
+    w = mi.workload(1)
+    dw = make(w)
+    with pytest.raises(C.MLAError):
+        C.mla_decode_fwd(dw.q_cat, dw.kv, dw.block_table, dw.seq_lens, dw.num_parts, dw.o_part,
+                         dw.lse_part, dev_status=dw.status,
+                         flags=C.MLA_DECODE_TEST_WAIT_TIMEOUT)
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["auto", "simt"])
+def test_length_beyond_the_table_is_clamped_and_reported(flags):
+    # a length past max_blocks_per_seq * block_size is clamped to the table
+    # and reported as MLA_DEV_BAD_LENGTH; the result equals the clamped length's
+    from mla_latent_kv_72_b300 import binding as C
+    w = mi.scaled(mi.workload(3), B=3, h=16, L=640)
+    dw = make(w, num_parts=4)
+    dw.step(flags=flags)
+    torch.cuda.synchronize()
+    ref_out = dw.out.clone()
+    dw.seq_lens[1] = 640 + 64 * 5
+    dw.status.zero_()
+    dw.attend(flags=flags)
+    torch.cuda.synchronize()
+    assert dw.check_status() == C.MLA_DEV_BAD_LENGTH
+    dw.seq_lens[1] = 640
+    dw.combine()
+    dw.project()
+    torch.cuda.synchronize()
+    assert torch.equal(dw.out.view(torch.int32), ref_out.view(torch.int32))
