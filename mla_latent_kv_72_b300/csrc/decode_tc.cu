@@ -96,7 +96,7 @@ constexpr int kQRopeBytes = 128 * 64;       // query RoPE slice: 128 heads x 32 
 constexpr int kXChunks = 16;                // 16-byte chunks per row
 constexpr int kRecvBytes = 128 * kXChunks * 16;
 
-constexpr int kNumBars = 32;
+constexpr int kNumBars = 40;
 
 // Layout of one variant: the bf16 cache (4 stages) or the FP8 latent cache (3
 // bf16 stages filled by converter warps from 2 FP8 landing buffers).
@@ -155,7 +155,8 @@ enum {
   BAR_DRAIN = BAR_SEG + 1,
   BAR_DRAIN_O = BAR_DRAIN + 1,          // bf16 variant: the P.C issuer's own drain
   BAR_NEVER = BAR_DRAIN_O + 1,          // signalled by nothing (diagnostic timeout wait)
-  BAR_COUNT = BAR_NEVER + 1,
+  BAR_QTMA = BAR_NEVER + 1,             // TMA of the query RoPE slice landed (its issuer waits)
+  BAR_COUNT = BAR_QTMA + 1,
 };
 static_assert(BAR_COUNT <= kNumBars, "barrier array");
 
@@ -276,16 +277,23 @@ __device__ unsigned long long* g_trace = nullptr;
   } while (0)
 #endif
 
-// Walks the part's tiles (sequence b, logical block blk) in stream order.
+// Walks the part's tiles (sequence b, logical block blk) in stream order.  The
+// current sequence's clamped length is kept, so that a tile's valid length
+// needs no memory access (the length is loaded once, when the walk enters the
+// sequence).
 struct TileIter {
   const int32_t* lens;
-  int maxb, b, blk, nb;
+  int maxb, b, blk, nb, L;
+  __device__ static int clamp_len(int L, int maxb) {
+    return L < 0 ? 0 : (L > maxb * kTok ? maxb * kTok : L);
+  }
   __device__ void init(const int32_t* l, int max_blocks, int b0, int blk0) {
     lens = l;
     maxb = max_blocks;
     b = b0;
     blk = blk0;
-    nb = seq_blocks(lens, b, kTok, maxb);
+    L = clamp_len(lens[b], maxb);
+    nb = (L + kTok - 1) / kTok;
   }
   // only called while another tile of the part follows, so b stays < B
   __device__ void next() {
@@ -293,16 +301,14 @@ struct TileIter {
       blk = 0;
       do {
         ++b;
-        nb = seq_blocks(lens, b, kTok, maxb);
+        L = clamp_len(lens[b], maxb);
+        nb = (L + kTok - 1) / kTok;
       } while (nb == 0);
     }
   }
-  __device__ int len() const {
-    int L = lens[b];
-    return L < 0 ? 0 : (L > maxb * kTok ? maxb * kTok : L);
-  }
+  __device__ int len() const { return L; }
   __device__ int valid() const {
-    const int n = len() - blk * kTok;
+    const int n = L - blk * kTok;
     return n < kTok ? n : kTok;
   }
 };
@@ -351,7 +357,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     }
     for (int i = 0; i < 4; ++i) mbar_init(bar(BAR_O_DONE + i), 1);
     mbar_init(bar(BAR_Q_FREE), 1);
-    mbar_init(bar(BAR_Q_READY), kSoftWarps + 1);
+    mbar_init(bar(BAR_Q_READY), kSoftWarps);
+    mbar_init(bar(BAR_QTMA), 1);
     mbar_init(bar(BAR_O_FREE), kSoftWarps);
     mbar_init(bar(BAR_SEG), kSoftWarps);
     mbar_init(bar(BAR_DRAIN), 1);
@@ -877,11 +884,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     const bool q32 = (reinterpret_cast<uintptr_t>(p.q_cat) & 31u) == 0;
     const bool o32 = (reinterpret_cast<uintptr_t>(p.o_part) & 31u) == 0;
     static_assert(kQChunks * kGroups * kHalves == 8, "query chunks per thread");
+    int n_qtma = 0;  // query RoPE loads issued by this thread (group lead of group 0)
     auto load_q = [&](int b) {
       if (group_lead && g == 0) {
         // RoPE dims [512 + 32 rank, +32) of the 128 query rows of sequence b
-        mbar_arrive_expect_tx(bar(BAR_Q_READY), kQRopeBytes);
-        tma_load_2d(sbase + kOffQRope, &tm_q, 512 + 32 * (int)rank, b * p.h, bar(BAR_Q_READY));
+        mbar_arrive_expect_tx(bar(BAR_QTMA), kQRopeBytes);
+        tma_load_2d(sbase + kOffQRope, &tm_q, 512 + 32 * (int)rank, b * p.h, bar(BAR_QTMA));
       }
       const uint4* q = reinterpret_cast<const uint4*>(p.q_cat + ((int64_t)b * p.h + (live ? row : 0)) * 576);
       const int qc0 = (g * kHalves + hf) * kQChunks;
@@ -913,6 +921,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       for (int cc = 0; cc < kQChunks; ++cc) tmem_st16(tl + kColQ + 16 * (qc0 + cc), w[cc]);
       tmem_wait_st();
       tc_fence_before();
+      if (group_lead && g == 0) {
+        // the issuer sees its own copy land before it signals the MMA warp, so
+        // no copy into this CTA's shared memory is in flight once the role
+        // ends, whatever the other roles do (no abort: the copy always lands)
+        int never = 0;
+        bool dummy = false;
+        mbar_wait_or_abort(bar(BAR_QTMA), n_qtma & 1, lim, &never, &dummy);
+        ++n_qtma;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_Q_READY));
     };
