@@ -454,6 +454,8 @@ def run_ours(args) -> None:
     e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3)
     e2e_value = aggregate(step_bytes * e2e_steps, world, e2e_s) / 1e9
 
+    append = time_append(dw, stream, n_st)
+
     if rank != 0:
         return
     peaks, peak_kind = load_peaks()
@@ -496,12 +498,72 @@ def run_ours(args) -> None:
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
+        "append": append,
         "gpu_launches": 4 * n_st,
         "clocks": clocks,
         "settle_s": args.settle_s,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
+
+
+def time_append(dw, stream, steps: int) -> dict:
+    """Per-launch time of mla_cache_append (one token per sequence), the
+    cache write of each decode step: every call rewrites each sequence's last
+    token (position L_b - 1) with its own data, so the cache is unchanged."""
+    import numpy as np
+    import torch
+
+    import mla_inputs as mi
+    from mla_latent_kv_72_b300 import binding as C
+    from mla_latent_kv_72_b300.workload import storage_to_torch
+    w = dw.w
+    last = [mi.sequence_last_row(w, b, int(dw.lens_np[b])) for b in range(w.B)]
+    c = np.stack([r[0] for r in last])
+    kr = np.stack([r[1] for r in last])
+    c_t = storage_to_torch(c, mi.latent_source_dtype(w), dw.device)
+    kr_t = storage_to_torch(kr, w.dtype, dw.device)
+    pos = torch.from_numpy((dw.lens_np - 1).astype(np.int32)).to(dw.device)
+    def launch():
+        C.mla_cache_append(c_t, kr_t, pos, dw.block_table, dw.kv, rope_theta=w.theta,
+                           dev_status=dw.status)
+
+    # the launches are replayed from a CUDA graph, so that the events time the
+    # GPU work and not the host's launch overhead (a lone small kernel on an
+    # idle GPU would otherwise wait for its own launch)
+    per_graph = 50
+    for _ in range(3):
+        launch()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        launch()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            launch()
+    torch.cuda.synchronize()
+    n = max(3, min(steps // 10, 20))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for a, b in ev:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    assert dw.check_status() == 0
+    us = [a.elapsed_time(b) * 1e3 / per_graph for a, b in ev]
+    per_tok = C.mla_cache_bytes_per_token(
+        {"f32": 0, "bf16": 1, "fp8e4m3": 2}[w.latent_dtype], 0 if w.dtype == "f32" else 1,
+        w.d_c, w.d_r, w.block_size)
+    return {"kernel": "mla_cache_append", "tokens_per_launch": w.B,
+            "mean_us": statistics.fmean(us), "median_us": statistics.median(us),
+            "min_us": min(us), "written_bytes_per_launch": w.B * per_tok,
+            "position": "each sequence's last token rewritten with its own data",
+            "timing": f"CUDA events around graph replays of {per_graph} launches"}
 
 
 def main(argv=None) -> None:

@@ -18,7 +18,8 @@
  *                                       balanced parts of all sequences' blocks)
  *   mla_combine    -> o_lat, lse       (log-sum-exp merge of the splits)
  *   mla_out_proj   -> out              (W_UV applied after attention)
- * plus two preparation/test helpers (mla_cache_fill, mla_paged_gather).
+ * plus the per-step cache write (mla_cache_append) and two preparation/test
+ * helpers (mla_cache_fill, mla_paged_gather).
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
@@ -292,6 +293,37 @@ int mla_cache_fill(const void* c_kv, const void* k_rope, int src_dtype,
                    const int32_t* cu_seqlens, int B, int max_len, const int32_t* block_table,
                    int max_blocks_per_seq, const mla_kv_cache* kv, double rope_theta,
                    int32_t* dev_status, void* stream);
+
+/*
+ * mla_cache_append: the per-step cache write of decoding - one new token per
+ * sequence (iotdigitaltwinplm.com, the absorbed-decode listing in "A latent
+ * KV projection in PyTorch": the new c and rotated k_R are appended before
+ * attention; "Interaction with quantisation and paging": paged blocks, FP8
+ * latent; intvml.com "DL0107 MLA": the RoPE key is cached in rotated form).
+ * For sequence b, with t = pos[b] (the token's position = the sequence's
+ * length before the append; the caller raises seq_lens afterwards), the row
+ * goes to physical block block_table[b, t / block_size], slot t % block_size:
+ *   latent row = c_new[b]                 (F32/BF16 cache: copied)
+ *   rope row   = RoPE(k_rope_new[b], t)   (as in mla_cache_fill)
+ * FP8 latent (the cache keeps only codes and one float32 scale per block):
+ *   - slot 0 (an empty block): scale = amax(row) / 448 (1 if 0), code =
+ *     e4m3(c / scale), as mla_cache_fill quantises a one-row block;
+ *   - otherwise, with a = amax(row) and s = scale[p]: if a <= 448 s (float32
+ *     product) the scale stays and code = e4m3(c / s); else the scale grows to
+ *     s' = a / 448, every earlier code of the block becomes
+ *     e4m3((e4m3(code) * s) / s') (float32 steps) and code = e4m3(c / s').
+ *   Rounding is to nearest even, saturating to +-448, as in mla_cache_fill.
+ *   c_new [B, d_c]: src_dtype (MLA_F32, or MLA_BF16 for BF16/FP8 caches)
+ *   k_rope_new [B, d_r]: the cache's rope dtype, unrotated
+ *   pos [B] int32 device array; block_table [B, max_blocks_per_seq] int32
+ * A position outside [0, max_blocks_per_seq * block_size) or a block-table
+ * entry outside the pool is skipped and reported in *dev_status.  Sequences
+ * must not share physical blocks (CTA b owns its block for the call).
+ */
+int mla_cache_append(const void* c_new, const void* k_rope_new, int src_dtype,
+                     const int32_t* pos, int B, const int32_t* block_table,
+                     int max_blocks_per_seq, const mla_kv_cache* kv, double rope_theta,
+                     int32_t* dev_status, void* stream);
 
 /*
  * mla_paged_gather: copy each sequence's logical rows out of the pool, bit for

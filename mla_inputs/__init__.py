@@ -210,6 +210,12 @@ def sequence(w: Workload, b: int, L: int) -> tuple[np.ndarray, np.ndarray]:
     return to_storage(c, latent_source_dtype(w)), to_storage(kr, w.dtype)
 
 
+def sequence_last_row(w: Workload, b: int, L: int) -> tuple[np.ndarray, np.ndarray]:
+    """Storage form of the last row (index L - 1) of sequence(w, b, L)."""
+    c, kr = sequence(w, b, L)
+    return c[L - 1], kr[L - 1]
+
+
 def queries(w: Workload) -> tuple[np.ndarray, np.ndarray]:
     """Storage form of q_nope [B, h, d_nope] and unrotated q_rope [B, h, d_r]."""
     rng = np.random.default_rng([w.seed, TAG_Q])

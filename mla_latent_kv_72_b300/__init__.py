@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     library_path,
     mla_absorb_q,
     mla_cache_bytes_per_token,
+    mla_cache_append,
     mla_cache_fill,
     mla_combine,
     mla_decode_fwd,

@@ -30,7 +30,7 @@ _LIB = None
 EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_version", "mla_cache_bytes_per_token", "mla_absorb_q",
     "mla_decode_num_partials", "mla_decode_fwd", "mla_combine", "mla_decode_attend_noalloc",
-    "mla_out_proj", "mla_cache_fill", "mla_paged_gather",
+    "mla_out_proj", "mla_cache_fill", "mla_cache_append", "mla_paged_gather",
 )
 
 
@@ -109,6 +109,7 @@ def lib() -> ctypes.CDLL:
                                             vp, vp, vp]),
         "mla_out_proj": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
         "mla_cache_fill": (i32, [vp, vp, i32, vp, i32, i32, vp, i32, kvp, f64, vp, vp]),
+        "mla_cache_append": (i32, [vp, vp, i32, vp, i32, vp, i32, kvp, f64, vp, vp]),
         "mla_paged_gather": (i32, [kvp, vp, i32, vp, i32, i32, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -233,6 +234,16 @@ def mla_cache_fill(c_kv, k_rope, cu_seqlens, max_len, block_table, kv: KVCache,
         _ptr(c_kv), _ptr(k_rope), dtype_code(c_kv.dtype), _ptr(cu_seqlens), B, int(max_len),
         _ptr(block_table), block_table.shape[1], ctypes.byref(kv), float(rope_theta),
         _ptr(dev_status), _stream(stream)))
+
+
+def mla_cache_append(c_new, k_rope_new, pos, block_table, kv: KVCache, rope_theta=10000.0,
+                     dev_status=None, stream=None):
+    """Append one token per sequence at position pos[b] (see mla72.h)."""
+    B = c_new.shape[0]
+    _check("mla_cache_append", lib().mla_cache_append(
+        _ptr(c_new), _ptr(k_rope_new), dtype_code(c_new.dtype), _ptr(pos), B, _ptr(block_table),
+        block_table.shape[1], ctypes.byref(kv), float(rope_theta), _ptr(dev_status),
+        _stream(stream)))
 
 
 def mla_paged_gather(kv: KVCache, block_table, cu_seqlens, max_len, latent_out=None,

@@ -166,6 +166,23 @@ int mla_cache_fill(const void* c_kv, const void* k_rope, int src_dtype,
                                           dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+int mla_cache_append(const void* c_new, const void* k_rope, int src_dtype, const int32_t* pos,
+                     int B, const int32_t* block_table, int max_blocks_per_seq,
+                     const mla_kv_cache* kv, double rope_theta, int32_t* dev_status,
+                     void* stream) {
+  if (!c_new || !k_rope || !pos || !block_table) return MLA_ERR_ARG;
+  if (B <= 0 || max_blocks_per_seq <= 0 || !(rope_theta > 0.0)) return MLA_ERR_ARG;
+  int st = check_cache(kv);
+  if (st != MLA_OK) return st;
+  if (!is_float_dtype(src_dtype)) return MLA_ERR_DTYPE;
+  if (kv->latent_dtype == MLA_FP8E4M3 ? src_dtype != MLA_BF16 : src_dtype != kv->latent_dtype)
+    return MLA_ERR_DTYPE;
+  if (!aligned16(c_new) || !aligned16(k_rope)) return MLA_ERR_ALIGN;
+  return from_cuda(mla::launch_cache_append(c_new, k_rope, src_dtype, pos, B, block_table,
+                                            max_blocks_per_seq, *kv, rope_theta, dev_status,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 int mla_paged_gather(const mla_kv_cache* kv, const int32_t* block_table, int max_blocks_per_seq,
                      const int32_t* cu_seqlens, int B, int max_len, void* latent_out,
                      void* rope_out, int32_t* dev_status, void* stream) {

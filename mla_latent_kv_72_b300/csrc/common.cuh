@@ -184,6 +184,11 @@ cudaError_t launch_cache_fill(const void* c_kv, const void* k_rope, int src_dtyp
                               const mla_kv_cache& kv, double theta, int32_t* status,
                               cudaStream_t s);
 
+cudaError_t launch_cache_append(const void* c_new, const void* k_rope, int src_dtype,
+                                const int32_t* pos, int B, const int32_t* block_table,
+                                int max_blocks, const mla_kv_cache& kv, double theta,
+                                int32_t* status, cudaStream_t s);
+
 cudaError_t launch_paged_gather(const mla_kv_cache& kv, const int32_t* block_table,
                                 int max_blocks, const int32_t* cu_seqlens, int B, int max_len,
                                 void* latent_out, void* rope_out, int32_t* status,

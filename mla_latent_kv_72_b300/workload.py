@@ -29,13 +29,17 @@ class DeviceWorkload:
     """Everything one decode step reads and writes, resident on one GPU."""
 
     def __init__(self, w: mi.Workload, device="cuda", num_parts: int | None = None,
-                 rows_per_upload: int = 1 << 20, out_dtype=torch.float32):
+                 rows_per_upload: int = 1 << 20, out_dtype=torch.float32,
+                 fill_lens: np.ndarray | None = None):
         self.w = w
         self.device = torch.device(device)
         dev = self.device
         lens = mi.lengths(w)
         table, nblk = mi.block_table(w, lens)
         self.lens_np = lens
+        # rows written at set-up (the rest are appended by append_tail)
+        self.fill_np = lens.copy() if fill_lens is None else np.minimum(
+            np.asarray(fill_lens, dtype=np.int64), lens)
         self.table_np = table
         self.num_blocks = nblk
         self.max_len = int(lens.max())
@@ -82,26 +86,54 @@ class DeviceWorkload:
         w = self.w
         src_dt = mi.latent_source_dtype(w)
         b = 0
+        fl = self.fill_np
         while b < w.B:
             e, rows = b, 0
-            while e < w.B and (e == b or rows + self.lens_np[e] <= rows_per_upload):
-                rows += int(self.lens_np[e])
+            while e < w.B and (e == b or rows + fl[e] <= rows_per_upload):
+                rows += int(fl[e])
                 e += 1
+            if rows == 0:
+                b = e
+                continue
             cs, krs = [], []
             for bb in range(b, e):
                 c, kr = mi.sequence(w, bb, int(self.lens_np[bb]))
-                cs.append(c)
-                krs.append(kr)
+                cs.append(c[: fl[bb]])
+                krs.append(kr[: fl[bb]])
             c_t = storage_to_torch(np.concatenate(cs), src_dt, self.device)
             kr_t = storage_to_torch(np.concatenate(krs), w.dtype, self.device)
             cu = np.zeros(e - b + 1, dtype=np.int32)
-            cu[1:] = np.cumsum(self.lens_np[b:e])
+            cu[1:] = np.cumsum(fl[b:e])
             cu_t = torch.from_numpy(cu).to(self.device)
             tab = self.block_table[b:e].contiguous()
-            C.mla_cache_fill(c_t, kr_t, cu_t, int(self.lens_np[b:e].max()), tab, self.kv,
+            C.mla_cache_fill(c_t, kr_t, cu_t, int(max(1, fl[b:e].max())), tab, self.kv,
                              rope_theta=w.theta, dev_status=self.status)
             b = e
         torch.cuda.synchronize(self.device)
+
+    def append_tail(self) -> int:
+        """Append the rows past the set-up fill one token per call: call s
+        appends row fill_b + s of every sequence that still has one, through
+        mla_cache_append.  Returns the number of calls."""
+        w = self.w
+        src_dt = mi.latent_source_dtype(w)
+        todo = self.lens_np - self.fill_np
+        seqs = {b: mi.sequence(w, b, int(self.lens_np[b])) for b in range(w.B) if todo[b] > 0}
+        calls = 0
+        for step in range(int(todo.max()) if len(todo) else 0):
+            bs = [b for b in range(w.B) if todo[b] > step]
+            t = [int(self.fill_np[b]) + step for b in bs]
+            c = np.stack([seqs[b][0][tt] for b, tt in zip(bs, t)])
+            kr = np.stack([seqs[b][1][tt] for b, tt in zip(bs, t)])
+            idx = torch.tensor(bs, dtype=torch.long, device=self.device)
+            C.mla_cache_append(storage_to_torch(c, src_dt, self.device),
+                               storage_to_torch(kr, w.dtype, self.device),
+                               torch.tensor(t, dtype=torch.int32, device=self.device),
+                               self.block_table.index_select(0, idx).contiguous(), self.kv,
+                               rope_theta=w.theta, dev_status=self.status)
+            calls += 1
+        torch.cuda.synchronize(self.device)
+        return calls
 
     # -- the decode step ---------------------------------------------------
     def absorb(self, stream=None):

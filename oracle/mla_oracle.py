@@ -335,6 +335,74 @@ def quantized_latent_f64(c_src32: np.ndarray, block_size: int) -> tuple[np.ndarr
     return codes, scales, deq
 
 
+def fp8_append_row(codes, scale, c_new):
+    """Append one latent row to an FP8 block that already holds len(codes) rows.
+
+    The cache keeps only the e4m3 codes and the block's float32 scale, so the
+    block's earlier values are known only in dequantised form.  Reading of
+    iotdigitaltwinplm.com "Interaction with quantisation and paging" (the
+    latent is stored in FP8 and the cache grows by one token per decode step):
+
+    * an empty block (the token lands in slot 0) is quantised on its own, as
+      ``fp8_quantize_block`` does for one row;
+    * otherwise, with a = max|c_new| and s the block's scale, the scale stays
+      when a <= 448 s (float32 product): the new row's code is e4m3(c / s);
+    * when a > 448 s the scale grows to s' = a / 448 (float32 quotient), every
+      earlier code is re-quantised from its dequantised value,
+      e4m3((e4m3(code) * s) / s') (each step a float32 operation), and the new
+      row's code is e4m3(c / s').
+
+    codes [rows, d_c] uint8, scale float32, c_new [d_c] (float32 values).
+    Returns (codes [rows + 1, d_c], new scale).
+    """
+    codes = np.asarray(codes, dtype=np.uint8).reshape(-1, np.asarray(c_new).shape[-1])
+    x = np.asarray(c_new, dtype=np.float32)
+    if codes.shape[0] == 0:
+        c, sc = fp8_quantize_block(x[None, :])
+        return c, sc
+    s_old = np.float32(scale)
+    a = np.float32(np.max(np.abs(x)))
+    if a > np.float32(E4M3_MAX) * s_old:
+        s_new = np.float32(a / np.float32(E4M3_MAX))
+        deq = (e4m3_decode(codes).astype(np.float32) * s_old).astype(np.float32)
+        old = e4m3_encode((deq / s_new).astype(np.float32).astype(np.float64))
+    else:
+        s_new = s_old
+        old = codes
+    new = e4m3_encode((x / s_new).astype(np.float32).astype(np.float64))
+    return np.concatenate([old, new[None, :]], axis=0), s_new
+
+
+def quantized_latent_appended(c_src32, block_size, n_fill):
+    """FP8 latent of a sequence whose first n_fill rows were written block by
+    block (``fp8_quantize_block`` over each block's rows) and whose remaining
+    rows were appended one at a time (``fp8_append_row``).
+
+    Returns (codes [L, d_c] uint8, scales [nblocks] float32, dequantised [L, d_c] f64).
+    """
+    c_src32 = np.asarray(c_src32, dtype=np.float32)
+    L = c_src32.shape[0]
+    nb = (L + block_size - 1) // block_size
+    codes = np.zeros(c_src32.shape, dtype=np.uint8)
+    scales = np.zeros(nb, dtype=np.float32)
+    for j in range(nb):
+        r0, r1 = j * block_size, min(L, (j + 1) * block_size)
+        f1 = min(r1, max(r0, n_fill))                # rows [r0, f1) come from the fill
+        if f1 > r0:
+            blk, sc = fp8_quantize_block(c_src32[r0:f1])
+        else:
+            blk, sc = np.zeros((0, c_src32.shape[1]), dtype=np.uint8), np.float32(1.0)
+        for r in range(f1, r1):
+            blk, sc = fp8_append_row(blk, sc, c_src32[r])
+        codes[r0:r1] = blk
+        scales[j] = sc
+    deq = np.zeros(c_src32.shape, dtype=np.float64)
+    for j in range(nb):
+        r0, r1 = j * block_size, min(L, (j + 1) * block_size)
+        deq[r0:r1] = fp8_dequantize(codes[r0:r1], scales[j])
+    return codes, scales, deq
+
+
 # ----------------------------------------------------------------------------
 # paged cache, logical view
 # ----------------------------------------------------------------------------
@@ -352,11 +420,13 @@ def paged_gather(pool: np.ndarray, table_row: np.ndarray, L: int, block_size: in
 # the oracle's view of a seeded workload
 # ----------------------------------------------------------------------------
 
-def sequence_view(w, b: int, L: int):
+def sequence_view(w, b: int, L: int, n_fill: int | None = None):
     """(c_kv f64 [L, d_c], unrotated k_rope f64 [L, d_r]) exactly as the cache holds them.
 
     bf16 / f32 latents are the stored values; an FP8 latent is the
-    dequantised value of the per-block e4m3 codes (``quantized_latent_f64``).
+    dequantised value of the per-block e4m3 codes (``quantized_latent_f64``,
+    or ``quantized_latent_appended`` when only the first n_fill rows were
+    written block by block and the rest appended one at a time).
     """
     import mla_inputs as mi
     c_st, kr_st = mi.sequence(w, b, L)
@@ -364,7 +434,10 @@ def sequence_view(w, b: int, L: int):
     src = mi.latent_source_dtype(w)
     if w.latent_dtype == "fp8e4m3":
         c32 = mi.storage_to_f64(c_st, src).astype(np.float32)
-        _, _, c = quantized_latent_f64(c32, w.block_size)
+        if n_fill is None or n_fill >= L:
+            _, _, c = quantized_latent_f64(c32, w.block_size)
+        else:
+            _, _, c = quantized_latent_appended(c32, w.block_size, n_fill)
     else:
         c = mi.storage_to_f64(c_st, src)
     return c, kr

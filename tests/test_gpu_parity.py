@@ -421,3 +421,73 @@ def test_length_beyond_the_table_is_clamped_and_reported(flags):
     dw.project()
     torch.cuda.synchronize()
     assert torch.equal(dw.out.view(torch.int32), ref_out.view(torch.int32))
+
+
+# ----------------------------------------------------------------------------
+# the per-step cache append (one token per sequence per call)
+# ----------------------------------------------------------------------------
+
+APPEND_CASES = {
+    "bf16_contiguous": mi.scaled(mi.workload(3), B=3, h=16, L=None, L_range=(70, 300),
+                                 layout="contiguous"),
+    "bf16_paged": mi.scaled(mi.workload(4), B=4, h=16, L_range=(70, 300)),
+    "fp8": mi.scaled(mi.workload(5), B=3, h=16, L=None, L_range=(70, 300)),
+}
+
+
+@pytest.mark.parametrize("name", list(APPEND_CASES))
+def test_cache_append_matches_oracle(name):
+    # each sequence is filled to L - k rows (k crosses a block boundary) and
+    # its last k rows are appended one token per call; the cache must then
+    # hold the oracle's append result bit for bit (codes and scales for the
+    # FP8 latent; the rotated keys equal the fill's), and the decode over it
+    # must match the oracle
+    w = APPEND_CASES[name]
+    lens = mi.lengths(w)
+    k = np.array([40, 65, 1, 64][: w.B])[: w.B]
+    fill = np.maximum(lens - k, 0)
+    dw = make(w, fill_lens=fill, num_parts=5)
+    ref = make(w, num_parts=5)                  # the same rows, filled at once
+    calls = dw.append_tail()
+    assert calls == int((lens - fill).max())
+    assert dw.check_status() == 0
+    lat, rope, cu = _gather(dw)
+    lat_f, rope_f, _ = _gather(ref)
+    np.testing.assert_array_equal(rope, rope_f)                 # same rotation arithmetic
+    src_dt = mi.latent_source_dtype(w)
+    for b in range(w.B):
+        L = int(lens[b])
+        c_src, _ = mi.sequence(w, b, L)
+        got = lat[cu[b]:cu[b + 1]]
+        if w.latent_dtype == "fp8e4m3":
+            c32 = mi.storage_to_f64(c_src, src_dt).astype(np.float32)
+            codes, scales, _ = O.quantized_latent_appended(c32, w.block_size, int(fill[b]))
+            np.testing.assert_array_equal(got.numpy(), codes)
+            sc = dw.scale.cpu().numpy()[dw.table_np[b, : len(scales)]]
+            np.testing.assert_array_equal(sc, scales)
+        else:
+            ref_rows = lat_f[cu[b]:cu[b + 1]]
+            bits = torch.int16 if got.element_size() == 2 else torch.int32
+            assert torch.equal(got.view(bits), ref_rows.view(bits))
+    dw.step()
+    torch.cuda.synchronize()
+    assert dw.check_status() == 0
+    inp = O.workload_inputs_f64(w)
+    seqs = [O.sequence_view(w, b, int(lens[b]), n_fill=int(fill[b])) for b in range(w.B)]
+    oref = O.decode_reference(inp["q_nope"], inp["q_rope"], inp["q_pos"], inp["w_uk"],
+                              inp["w_uv"], seqs)
+    check_against(oref, dw, range(w.B), None, TOL["bf16"])
+
+
+def test_cache_append_reports_bad_positions():
+    from mla_latent_kv_72_b300 import binding as C
+    w = mi.scaled(mi.workload(3), B=2, h=16, L=100)
+    dw = make(w)
+    c = torch.zeros((2, 512), dtype=torch.bfloat16, device="cuda")
+    kr = torch.zeros((2, 64), dtype=torch.bfloat16, device="cuda")
+    before = dw.pool.clone()
+    pos = torch.tensor([-1, 64 * dw.block_table.shape[1]], dtype=torch.int32, device="cuda")
+    C.mla_cache_append(c, kr, pos, dw.block_table, dw.kv, dev_status=dw.status)
+    torch.cuda.synchronize()
+    assert dw.check_status() == C.MLA_DEV_BAD_LENGTH
+    assert torch.equal(dw.pool.view(torch.int16), before.view(torch.int16))   # nothing written

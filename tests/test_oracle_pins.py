@@ -529,3 +529,86 @@ def test_quantized_latent_blocks_follow_the_rows():
     assert O.e4m3_decode(codes[5, 3]) == 448.0
     assert O.e4m3_decode(codes[127, 0]) == -448.0
     assert O.e4m3_decode(codes[128, 1]) == 448.0
+
+
+# ----------------------------------------------------------------------------
+# FP8 append (one token into a partly filled block)
+# ----------------------------------------------------------------------------
+
+def test_fp8_append_to_empty_block_is_block_quantisation():
+    x = np.random.default_rng(31).standard_normal(64).astype(np.float32)
+    codes, sc = O.fp8_append_row(np.zeros((0, 64), np.uint8), np.float32(1.0), x)
+    ref_codes, ref_sc = O.fp8_quantize_block(x[None, :])
+    np.testing.assert_array_equal(codes, ref_codes)
+    assert sc == ref_sc
+
+
+def test_fp8_append_hand_examples():
+    # block row [1, -2]: scale 2/448, codes 224 and -448
+    blk, s = O.fp8_quantize_block(np.array([[1.0, -2.0]], np.float32))
+    assert s == np.float32(2.0 / 448.0)
+    np.testing.assert_array_equal(O.e4m3_decode(blk), [[224.0, -448.0]])
+    # a smaller row keeps the scale and the earlier codes: 0.5 / (2/448) = 112
+    b2, s2 = O.fp8_append_row(blk, s, np.array([0.5, 0.0], np.float32))
+    assert s2 == s
+    np.testing.assert_array_equal(b2[0], blk[0])
+    np.testing.assert_array_equal(O.e4m3_decode(b2[1]), [112.0, 0.0])
+    # a row with amax 4 > 448 s = 2 grows the scale to 4/448: the earlier row
+    # re-quantises exactly to 112 and -224, the new one to 448 and 56
+    b3, s3 = O.fp8_append_row(blk, s, np.array([4.0, 0.5], np.float32))
+    assert s3 == np.float32(np.float32(4.0) / np.float32(448.0))
+    np.testing.assert_array_equal(O.e4m3_decode(b3), [[112.0, -224.0], [448.0, 56.0]])
+    # double rounding: row [3, 1] has codes 448 and e4m3(149.33) = 144; growing
+    # to 10/448 re-quantises 144 * (3/448) / (10/448) = 43.2 to 44
+    b4, s4 = O.fp8_quantize_block(np.array([[3.0, 1.0]], np.float32))
+    np.testing.assert_array_equal(O.e4m3_decode(b4), [[448.0, 144.0]])
+    b5, _ = O.fp8_append_row(b4, s4, np.array([10.0, 0.0], np.float32))
+    # 448 * (3/448) / (10/448) = 134.4 -> 128 (e4m3 steps of 16 there)
+    np.testing.assert_array_equal(O.e4m3_decode(b5[0]), [128.0, 44.0])
+
+
+def test_fp8_append_scale_matches_whole_block_quantisation():
+    # appending a block's rows one by one ends with the scale of quantising
+    # the block at once (amax of all rows / 448), whatever the row order
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((64, 48)).astype(np.float32)
+    x[17] *= np.float32(9.0)
+    blk, sc = np.zeros((0, 48), np.uint8), np.float32(1.0)
+    growths = 0
+    for r in range(64):
+        prev = sc
+        blk, sc = O.fp8_append_row(blk, sc, x[r])
+        growths += int(r > 0 and sc != prev)
+    assert growths >= 1
+    _, ref_sc = O.fp8_quantize_block(x)
+    assert sc == ref_sc
+    # rows appended after the largest one keep exactly the block quantiser's codes
+    ref_codes, _ = O.fp8_quantize_block(x)
+    np.testing.assert_array_equal(blk[17:], ref_codes[17:])
+    # a row is rounded once when appended and once more at each later growth
+    # of the scale: each rounding moves it by at most half an e4m3 step at the
+    # (final, coarsest) scale
+    deq = O.fp8_dequantize(blk, sc)
+    n_round = growths + 1
+    bound = (n_round * np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * float(sc)) * 1.1
+             + 1e-6 * float(sc))
+    assert np.all(np.abs(deq - x) <= bound)
+
+
+def test_quantized_latent_appended_reduces_to_the_fill():
+    rng = np.random.default_rng(33)
+    x = rng.standard_normal((150, 16)).astype(np.float32)
+    full = O.quantized_latent_f64(x, 64)
+    app = O.quantized_latent_appended(x, 64, 150)
+    for a, b in zip(full, app):
+        np.testing.assert_array_equal(a, b)
+    # filled to 100 rows, then 50 appended: blocks 0 (full) is untouched
+    codes, scales, _ = O.quantized_latent_appended(x, 64, 100)
+    np.testing.assert_array_equal(codes[:64], full[0][:64])
+    assert scales[0] == full[1][0]
+    # block 1 = rows 64..99 quantised together, then rows 100..127 appended
+    blk, sc = O.fp8_quantize_block(x[64:100])
+    for r in range(100, 128):
+        blk, sc = O.fp8_append_row(blk, sc, x[r])
+    np.testing.assert_array_equal(codes[64:128], blk)
+    assert scales[1] == sc
