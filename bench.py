@@ -224,8 +224,8 @@ def resolve_workload(arg):
     return mi.workload(arg)
 
 
-def bench_config(w, num_parts, l2_note) -> dict:
-    return {"workload": w.name, "B": w.B, "h": w.h, "L": w.L,
+def bench_config(w, num_parts, l2_note, q_len=1) -> dict:
+    return {"workload": w.name, "B": w.B, "h": w.h, "L": w.L, "q_len": q_len,
             "L_range": list(w.L_range) if w.L_range else None, "d_c": w.d_c, "d_r": w.d_r,
             "d_nope": w.d_nope, "d_v": w.d_v, "cache_dtype": w.latent_dtype,
             "layout": w.layout, "block_size": w.block_size, "num_parts": num_parts,
@@ -367,7 +367,12 @@ def run_ours(args) -> None:
     barrier()
     C.lib()
     w = resolve_workload(args.workload)
-    dw = DeviceWorkload(w, device=f"cuda:{local}", num_parts=args.parts)
+    parts = args.parts
+    if parts is None and args.q_len > 1:
+        # one CTA pair per part and per 128 query rows: keep one wave of pairs
+        groups = (args.q_len * w.h + 127) // 128
+        parts = max(1, C.default_num_parts(local) // groups)
+    dw = DeviceWorkload(w, device=f"cuda:{local}", num_parts=parts, q_len=args.q_len)
     stream = torch.cuda.current_stream()
 
     # inputs of one step smaller than L2 are flushed from it between timed
@@ -492,7 +497,7 @@ def run_ours(args) -> None:
         "warmup": args.warmup, "ms_per_step": 1e3 * max_total / n_st,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
-        "data": "synthetic", "config": bench_config(w, dw.num_parts, l2_note),
+        "data": "synthetic", "config": bench_config(w, dw.num_parts, l2_note, dw.q_len),
         "tflops": tflops, "steps_per_s": n_st / max_total,
         "step_ms": sstat,
         "roofline": roof,
@@ -576,6 +581,8 @@ def main(argv=None) -> None:
                    help="workload index 1..5 or name (default: the V3-shaped workload, 3)")
     p.add_argument("--parts", type=int, default=None,
                    help="balanced parts of the block stream (default: half the SM count)")
+    p.add_argument("--q-len", type=int, default=1,
+                   help="new tokens per sequence (multi-token decode; 1 = the one-token step)")
     p.add_argument("--settle-s", type=float, default=0.5,
                    help="seconds of untimed steps before the warm-up")
     p.add_argument("--cpu-budget", type=float, default=15.0,

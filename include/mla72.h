@@ -200,13 +200,45 @@ int mla_decode_num_partials(int B, int num_parts);
  * (BF16, BF16, BF16) and (BF16, FP8E4M3, BF16) on both kernels.  The tensor-core
  * kernel runs for d_c = 512, d_r = 64, block_size = 64, h <= 128; for an FP8
  * latent it dequantises each code to bf16(e4m3 value x block scale) before
- * the MMAs (relative rounding <= 2^-9 per element).
+ * the MMAs (relative rounding <= 2^-9 per element).  It runs one CTA pair per
+ * part and per 128 heads.
  * softmax_scale <= 0 selects 1/sqrt(d_nope + d_r) with d_nope = 128.
  */
 int mla_decode_fwd(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
                    const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
                    int B, int h, int num_parts, float softmax_scale, float* o_part,
                    float* lse_part, int32_t* dev_status, unsigned flags, void* stream);
+
+/* Largest q_len accepted by mla_decode_fwd_multi. */
+#define MLA_MAX_Q_LEN 8
+
+/*
+ * mla_decode_fwd_multi: attention of q_len new tokens per sequence (multi-
+ * token prediction, or speculative decoding verifying several drafted tokens
+ * in one step; iotdigitaltwinplm.com "Interaction with quantisation and
+ * paging" and "Arithmetic intensity changes under absorption": more query
+ * rows share each latent row read).  The L_b cached rows of sequence b
+ * include its q_len new tokens (appended first), so token j sits at position
+ * L_b - q_len + j and attends to rows 0 .. L_b - q_len + j (kexue.fm MHA
+ * equation: keys i <= t).  The query rows of a sequence are (j, s) at row
+ * j * h + s; everything else is as in mla_decode_fwd with h replaced by the
+ * q_len * h rows:
+ *   q_cat    [B, q_len, h, d_c + d_r] (mla_absorb_q with B * q_len query
+ *            rows and one position per token gives it)
+ *   o_part   [mla_decode_num_partials(B, num_parts), q_len * h, d_c] float32
+ *   lse_part [mla_decode_num_partials(B, num_parts), q_len * h] float32
+ * mla_combine with h = q_len * h merges the partials into o_lat
+ * [B, q_len, h, d_c].  A token that sees no row (L_b < q_len - j) gets
+ * o = 0 and lse = -inf.  Supported: 1 <= q_len <= MLA_MAX_Q_LEN,
+ * q_len * h <= 4096.  The tensor-core kernel runs a CTA pair per part and
+ * per 128 query rows: give it about (SM count / 2) / ceil(q_len h / 128)
+ * parts.
+ */
+int mla_decode_fwd_multi(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
+                         const int32_t* block_table, int max_blocks_per_seq,
+                         const int32_t* seq_lens, int B, int q_len, int h, int num_parts,
+                         float softmax_scale, float* o_part, float* lse_part,
+                         int32_t* dev_status, unsigned flags, void* stream);
 
 /*
  * mla_combine: merge the partials of mla_decode_fwd (log-sum-exp weighting;

@@ -20,6 +20,8 @@ regenerated on its own):
 * ``default_rng([seed, TAG_L])``: sequence lengths (variable-length workload).
 * ``default_rng([seed, TAG_P])``: the physical-block permutation of the
   paged workload.
+* ``default_rng([seed, TAG_QM, q_len])``: queries of q_len new tokens per
+  sequence (multi-token decode).
 
 All draws are float64; storage dtype "bf16" rounds f64 -> f32 -> bf16 with
 round-to-nearest-even at each step, "f32" rounds f64 -> f32.
@@ -36,6 +38,7 @@ TAG_Q = 12
 TAG_W = 13
 TAG_L = 14
 TAG_P = 15
+TAG_QM = 16
 
 
 # ----------------------------------------------------------------------------
@@ -106,6 +109,7 @@ class Workload:
     d_v: int = 128
     block_size: int = 64
     theta: float = 10000.0
+    lens: tuple[int, ...] | None = None   # explicit lengths (edge-case tests), else L / L_range
 
     @property
     def seed(self) -> int:
@@ -152,6 +156,9 @@ def scaled(w: Workload, **changes) -> Workload:
 
 def lengths(w: Workload) -> np.ndarray:
     """Cached length L_b of every sequence (int64 [B])."""
+    if w.lens is not None:
+        assert len(w.lens) == w.B
+        return np.asarray(w.lens, dtype=np.int64)
     if w.L is not None:
         return np.full(w.B, w.L, dtype=np.int64)
     lo, hi = w.L_range
@@ -208,6 +215,21 @@ def sequence(w: Workload, b: int, L: int) -> tuple[np.ndarray, np.ndarray]:
     """Storage form of sequence b's rows (latent source dtype, rope dtype)."""
     c, kr = sequence_f64(w, b, L)
     return to_storage(c, latent_source_dtype(w)), to_storage(kr, w.dtype)
+
+
+def queries_multi(w: Workload, q_len: int) -> tuple[np.ndarray, np.ndarray]:
+    """Storage form of q_nope [B, q_len, h, d_nope] and unrotated q_rope
+    [B, q_len, h, d_r] for q_len new tokens per sequence, standard normal."""
+    rng = np.random.default_rng([w.seed, TAG_QM, q_len])
+    qn = rng.standard_normal((w.B, q_len, w.h, w.d_nope))
+    qr = rng.standard_normal((w.B, q_len, w.h, w.d_r))
+    return to_storage(qn, w.dtype), to_storage(qr, w.dtype)
+
+
+def query_positions_multi(w: Workload, q_len: int, lens: np.ndarray | None = None) -> np.ndarray:
+    """Positions [B, q_len] of the new tokens: L_b - q_len + j."""
+    lens = lengths(w) if lens is None else lens
+    return (lens[:, None] - q_len + np.arange(q_len)[None, :]).astype(np.int32)
 
 
 def sequence_last_row(w: Workload, b: int, L: int) -> tuple[np.ndarray, np.ndarray]:

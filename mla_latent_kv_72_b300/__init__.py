@@ -21,6 +21,7 @@ from .binding import (  # noqa: F401
     mla_cache_fill,
     mla_combine,
     mla_decode_fwd,
+    mla_decode_fwd_multi,
     mla_decode_num_partials,
     mla_decode_attend_noalloc,
     default_num_parts,

@@ -29,7 +29,7 @@ _LIB = None
 
 EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_version", "mla_cache_bytes_per_token", "mla_absorb_q",
-    "mla_decode_num_partials", "mla_decode_fwd", "mla_combine", "mla_decode_attend_noalloc",
+    "mla_decode_num_partials", "mla_decode_fwd", "mla_decode_fwd_multi", "mla_combine", "mla_decode_attend_noalloc",
     "mla_out_proj", "mla_cache_fill", "mla_cache_append", "mla_paged_gather",
 )
 
@@ -104,6 +104,8 @@ def lib() -> ctypes.CDLL:
         "mla_absorb_q": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f64, vp]),
         "mla_decode_num_partials": (i32, [i32, i32]),
         "mla_decode_fwd": (i32, [vp, i32, kvp, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp, u32, vp]),
+        "mla_decode_fwd_multi": (i32, [vp, i32, kvp, vp, i32, vp, i32, i32, i32, i32, f32, vp, vp,
+                                       vp, u32, vp]),
         "mla_combine": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp]),
         "mla_decode_attend_noalloc": (i32, [vp, i32, kvp, vp, i32, vp, i32, i32, i32, f32, vp, i32,
                                             vp, vp, vp]),
@@ -190,6 +192,18 @@ def mla_decode_fwd(q_cat, kv: KVCache, block_table, seq_lens, num_parts, o_part,
     _check("mla_decode_fwd", lib().mla_decode_fwd(
         _ptr(q_cat), dtype_code(q_cat.dtype), ctypes.byref(kv), _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), B, h, int(num_parts), float(softmax_scale),
+        _ptr(o_part), _ptr(lse_part), _ptr(dev_status), int(flags), _stream(stream)))
+
+
+def mla_decode_fwd_multi(q_cat, kv: KVCache, block_table, seq_lens, num_parts, o_part, lse_part,
+                         *, softmax_scale=0.0, dev_status=None, flags=MLA_DECODE_AUTO,
+                         stream=None):
+    """Partials of q_len new tokens per sequence; q_cat [B, q_len, h, d_c + d_r],
+    o_part [slots, q_len * h, d_c], lse_part [slots, q_len * h] (see mla72.h)."""
+    B, q_len, h, _ = q_cat.shape
+    _check("mla_decode_fwd_multi", lib().mla_decode_fwd_multi(
+        _ptr(q_cat), dtype_code(q_cat.dtype), ctypes.byref(kv), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, q_len, h, int(num_parts), float(softmax_scale),
         _ptr(o_part), _ptr(lse_part), _ptr(dev_status), int(flags), _stream(stream)))
 
 

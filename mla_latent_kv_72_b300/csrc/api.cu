@@ -90,12 +90,18 @@ int mla_decode_num_partials(int B, int num_parts) {
   return B + num_parts - 1;
 }
 
-int mla_decode_fwd(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
-                   const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
-                   int B, int h, int num_parts, float softmax_scale, float* o_part,
-                   float* lse_part, int32_t* dev_status, unsigned flags, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks and dispatch shared by the one-token and the multi-token decode.
+int decode_impl(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
+                const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                int B, int q_len, int h, int num_parts, float softmax_scale, float* o_part,
+                float* lse_part, int32_t* dev_status, unsigned flags, void* stream) {
   if (!q_cat || !block_table || !seq_lens || !o_part || !lse_part) return MLA_ERR_ARG;
-  if (B <= 0 || h <= 0 || num_parts <= 0 || max_blocks_per_seq <= 0) return MLA_ERR_ARG;
+  if (B <= 0 || h <= 0 || q_len <= 0 || num_parts <= 0 || max_blocks_per_seq <= 0)
+    return MLA_ERR_ARG;
   if (flags != MLA_DECODE_AUTO && flags != MLA_DECODE_FORCE_SIMT &&
       flags != MLA_DECODE_TEST_WAIT_TIMEOUT)
     return MLA_ERR_ARG;
@@ -104,21 +110,44 @@ int mla_decode_fwd(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
   if (!is_float_dtype(q_dtype)) return MLA_ERR_DTYPE;
   if (q_dtype == MLA_F32 && kv->latent_dtype != MLA_F32) return MLA_ERR_DTYPE;
   if (q_dtype == MLA_BF16 && kv->latent_dtype == MLA_F32) return MLA_ERR_DTYPE;
-  if (num_parts > MLA_MAX_PARTS) return MLA_ERR_SHAPE;
+  if (num_parts > MLA_MAX_PARTS || q_len > MLA_MAX_Q_LEN || (int64_t)q_len * h > 4096)
+    return MLA_ERR_SHAPE;
   if (!aligned16(q_cat) || !aligned16(o_part)) return MLA_ERR_ALIGN;
   float scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / sqrt(128.0 + kv->d_r));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool tc = flags != MLA_DECODE_FORCE_SIMT && mla::decode_tc_supported(q_dtype, *kv, h);
+  const bool tc =
+      flags != MLA_DECODE_FORCE_SIMT && mla::decode_tc_supported(q_dtype, *kv, q_len * h);
   // the diagnostic timeout exists only in the pipelined tensor-core kernel
   if (flags == MLA_DECODE_TEST_WAIT_TIMEOUT && !tc) return MLA_ERR_ARG;
   if (tc) {
     return from_cuda(mla::launch_decode_tc(q_cat, *kv, block_table, max_blocks_per_seq, seq_lens,
-                                           B, h, num_parts, scale, o_part, lse_part, dev_status,
-                                           flags == MLA_DECODE_TEST_WAIT_TIMEOUT, s));
+                                           B, q_len, h, num_parts, scale, o_part, lse_part,
+                                           dev_status, flags == MLA_DECODE_TEST_WAIT_TIMEOUT, s));
   }
   return from_cuda(mla::launch_decode_simt(q_cat, q_dtype, *kv, block_table, max_blocks_per_seq,
-                                           seq_lens, B, h, num_parts, scale, o_part, lse_part,
-                                           dev_status, s));
+                                           seq_lens, B, q_len, h, num_parts, scale, o_part,
+                                           lse_part, dev_status, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_fwd(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
+                   const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                   int B, int h, int num_parts, float softmax_scale, float* o_part,
+                   float* lse_part, int32_t* dev_status, unsigned flags, void* stream) {
+  return decode_impl(q_cat, q_dtype, kv, block_table, max_blocks_per_seq, seq_lens, B, 1, h,
+                     num_parts, softmax_scale, o_part, lse_part, dev_status, flags, stream);
+}
+
+int mla_decode_fwd_multi(const void* q_cat, int q_dtype, const mla_kv_cache* kv,
+                         const int32_t* block_table, int max_blocks_per_seq,
+                         const int32_t* seq_lens, int B, int q_len, int h, int num_parts,
+                         float softmax_scale, float* o_part, float* lse_part,
+                         int32_t* dev_status, unsigned flags, void* stream) {
+  return decode_impl(q_cat, q_dtype, kv, block_table, max_blocks_per_seq, seq_lens, B, q_len, h,
+                     num_parts, softmax_scale, o_part, lse_part, dev_status, flags, stream);
 }
 
 int mla_combine(const float* o_part, const float* lse_part, const int32_t* seq_lens,

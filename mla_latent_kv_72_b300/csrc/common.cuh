@@ -149,12 +149,13 @@ cudaError_t launch_absorb_q_simt(const void* q_nope, const void* q_rope, const i
                                  const void* w_uk, void* q_cat, int B, int h, int d_nope,
                                  int d_c, int d_r, int dtype, double theta, cudaStream_t s);
 
+// q_len query tokens per sequence, heads heads each: q_len * heads query rows
 cudaError_t launch_decode_simt(const void* q_cat, int q_dtype, const mla_kv_cache& kv,
                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
-                               int B, int h, int num_parts, float scale, float* o_part,
-                               float* lse_part, int32_t* status, cudaStream_t s);
+                               int B, int q_len, int heads, int num_parts, float scale,
+                               float* o_part, float* lse_part, int32_t* status, cudaStream_t s);
 
-bool decode_tc_supported(int q_dtype, const mla_kv_cache& kv, int h);
+bool decode_tc_supported(int q_dtype, const mla_kv_cache& kv, int rows);
 
 // True on an sm_100-family device with the tensor-map encoder available.
 bool tc_device();
@@ -168,8 +169,9 @@ cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, i
 
 cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
-                             int B, int h, int num_parts, float scale, float* o_part,
-                             float* lse_part, int32_t* status, bool test_timeout, cudaStream_t s);
+                             int B, int q_len, int heads, int num_parts, float scale,
+                             float* o_part, float* lse_part, int32_t* status, bool test_timeout,
+                             cudaStream_t s);
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const int32_t* seq_lens,
                            int block_size, int max_blocks, int B, int h, int d_c, int num_parts,

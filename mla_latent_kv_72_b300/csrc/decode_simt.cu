@@ -23,7 +23,8 @@ struct SimtArgs {
   const int32_t* block_table;
   int max_blocks;
   const int32_t* seq_lens;
-  int B, h, num_parts;
+  int B, h, num_parts;   // h = q_len * heads query rows per sequence (row j * heads + s)
+  int heads, q_len;
   float scale;
   float* o_part;
   float* lse_part;
@@ -130,7 +131,10 @@ __global__ void __launch_bounds__(32 * kWarps) decode_simt_kernel(SimtArgs a) {
         const float* kr = sk + lane * ks;
         float acc = 0.f;
         for (int d = 0; d < dqk; ++d) acc = fmaf(qv[d], kr[d], acc);
-        float sc = (t0 + lane < t_end) ? acc * a.scale : -INFINITY;
+        // slots past the sequence end, and past this row's own position
+        // (token j = s / heads sits q_len - 1 - j before the last row), get -inf
+        const int lim = min(t_end, L - (a.q_len - 1 - s / a.heads));
+        float sc = (t0 + lane < lim) ? acc * a.scale : -INFINITY;
         float tmax = sc;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
@@ -173,10 +177,11 @@ __global__ void __launch_bounds__(32 * kWarps) decode_simt_kernel(SimtArgs a) {
 
 cudaError_t launch_decode_simt(const void* q_cat, int q_dtype, const mla_kv_cache& kv,
                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
-                               int B, int h, int num_parts, float scale, float* o_part,
-                               float* lse_part, int32_t* status, cudaStream_t s) {
+                               int B, int q_len, int heads, int num_parts, float scale,
+                               float* o_part, float* lse_part, int32_t* status, cudaStream_t s) {
+  const int h = q_len * heads;
   SimtArgs a{q_cat, q_dtype, kv, block_table, max_blocks, seq_lens, B, h, num_parts,
-             scale, o_part, lse_part, status};
+             heads, q_len, scale, o_part, lse_part, status};
   const int dqk = kv.d_c + kv.d_r;
   size_t smem = sizeof(float) * ((size_t)kWarps * dqk + (size_t)kTile * (dqk + 1));
   cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel,

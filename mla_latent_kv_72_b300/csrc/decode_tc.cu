@@ -168,7 +168,10 @@ struct TcParams {
   float* lse_part;              // [B + P - 1, h]
   int32_t* status;
   const float* kv_scale;        // FP8 variant: per-block dequantisation scale [num_blocks]
+  // rows of a sequence: h = q_len * heads query rows (token j, head s) at
+  // row j * heads + s; a CTA pair takes 128 of them (row group)
   int max_blocks, B, h, num_parts, num_blocks;
+  int heads, q_len;
   float scale_log2;
   long long wait_limit;
   // diagnostic: the MMA issuer's first wait is made on BAR_NEVER with this
@@ -330,7 +333,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int part = blockIdx.x / 2;
+  const int part = (blockIdx.x / 2) % p.num_parts;  // part of the block stream
+  const int row0 = (blockIdx.x / 2) / p.num_parts * 128;  // first query row of this pair
 
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8 * i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -466,8 +470,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
           if (pf.blk == 0 && kp > 0) {
             // a later segment starts here: its query rows (this CTA's latent
             // slice and RoPE dims) go to L2 ahead of the segment's query load
-            for (int j = 0; j < 8; ++j) tma_prefetch_2d(&tm_q, 256 * (int)rank + 32 * j, pf.b * p.h);
-            tma_prefetch_2d(&tm_q, 512 + 32 * (int)rank, pf.b * p.h);
+            for (int j = 0; j < 8; ++j)
+              tma_prefetch_2d(&tm_q, 256 * (int)rank + 32 * j, pf.b * p.h + row0);
+            tma_prefetch_2d(&tm_q, 512 + 32 * (int)rank, pf.b * p.h + row0);
           }
           if (kp + 1 < ntiles) pf.next();
         }
@@ -851,9 +856,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     const int g = (warp - 2) / kGroupWarps;   // group: tiles k with k % kGroups == g
     const int hf = wg >> 2;                   // column half: score columns [kCols hf, +kCols)
     const int sub = warp & 3;                 // TMEM sub-partition of this warp
-    const int row = sub * 32 + lane;          // head
+    const int row = sub * 32 + lane;          // TMEM lane: query row row0 + row
+    const int grow = row0 + row;
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
-    const bool live = row < p.h;
+    const bool live = grow < p.h;
+    // query token j = grow / heads sits q_len - 1 - j positions before the
+    // last cached row and sees the rows up to its own position
+    const int c_row = live ? p.q_len - 1 - grow / p.heads : 0;
     const bool group_lead = wg == 0 && lane == 0;
     float* mpub = reinterpret_cast<float*>(smem + kOffMpub);
     float* lm = reinterpret_cast<float*>(smem + C::kOffLm);
@@ -889,9 +898,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       if (group_lead && g == 0) {
         // RoPE dims [512 + 32 rank, +32) of the 128 query rows of sequence b
         mbar_arrive_expect_tx(bar(BAR_QTMA), kQRopeBytes);
-        tma_load_2d(sbase + kOffQRope, &tm_q, 512 + 32 * (int)rank, b * p.h, bar(BAR_QTMA));
+        tma_load_2d(sbase + kOffQRope, &tm_q, 512 + 32 * (int)rank, b * p.h + row0, bar(BAR_QTMA));
       }
-      const uint4* q = reinterpret_cast<const uint4*>(p.q_cat + ((int64_t)b * p.h + (live ? row : 0)) * 576);
+      const uint4* q = reinterpret_cast<const uint4*>(p.q_cat + ((int64_t)b * p.h + (live ? grow : 0)) * 576);
       const int qc0 = (g * kHalves + hf) * kQChunks;
       // all loads first (one memory round trip), then the TMEM stores; rows
       // are 1152 bytes apart, so each load instruction touches 32 lines:
@@ -1044,10 +1053,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         // the buffer may be refilled: tell the peer (the values are consumed)
         __syncwarp();
         if (lane == 0) mbar_arrive_remote_relaxed(peer_free);
-        if (n_valid < kTok) {  // ragged last block: slots past the end get -inf
+        // slots past the sequence end, and past this row's own position, get -inf
+        const int lim = min(n_valid, it.len() - it.blk * kTok - c_row);
+        if (lim < kTok) {
 #pragma unroll
           for (int kk = 0; kk < kCols; ++kk)
-            if (kCols * hf + kk >= n_valid) r[kk] = __float_as_uint(-INFINITY);
+            if (kCols * hf + kk >= lim) r[kk] = __float_as_uint(-INFINITY);
         }
 #pragma unroll
         for (int kk = 0; kk < kCols; ++kk) mt = fmaxf(mt, __uint_as_float(r[kk]));
@@ -1088,7 +1099,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
         // ---- P (bf16 pairs) in registers first, packed in place into r[0..kCols/2)
         f2_t psum2 = f2_make(0.f, 0.f);
-        const f2_t negm = f2_make(-m_k, -m_k);
+        // a row that sees no slot yet keeps m = -inf: its P is 0
+        const float nm = m_k == -INFINITY ? 0.f : -m_k;
+        const f2_t negm = f2_make(nm, nm);
 #pragma unroll
         for (int e = 0; e < kCols / 2; ++e) {
           const f2_t y = f2_add(f2_make(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), negm);
@@ -1179,8 +1192,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
         if (group_lead && g == 0) MLA_TR(k, 14);
         tc_fence_after();
         const int64_t slot = (int64_t)part + b;
-        float* orow = p.o_part + (slot * p.h + row) * 512 + rank * 256;
-        const float inv = 1.0f / l;
+        float* orow = p.o_part + (slot * p.h + (live ? grow : 0)) * 512 + rank * 256;
+        // a row that saw no slot of this segment: output 0, lse -inf (weight 0)
+        const float inv = l > 0.f ? 1.0f / l : 0.f;
         constexpr int kEpiChunks = 16 / (kGroups * kHalves);
         const int ec0 = (g * kHalves + hf) * kEpiChunks;
         for (int c = ec0; c < ec0 + kEpiChunks; ++c) {
@@ -1202,7 +1216,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             }
           }
         }
-        if (live && rank == 0 && g == 0 && hf == 0) p.lse_part[slot * p.h + row] = (M + log2f(l)) * kLn2;
+        if (live && rank == 0 && g == 0 && hf == 0)
+          p.lse_part[slot * p.h + grow] = l > 0.f ? (M + log2f(l)) * kLn2 : -INFINITY;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_O_FREE));
@@ -1313,10 +1328,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 bool tc_device() { return device_major() >= 10 && get_encode_fn() != nullptr; }
 
-bool decode_tc_supported(int q_dtype, const mla_kv_cache& kv, int h) {
+bool decode_tc_supported(int q_dtype, const mla_kv_cache& kv, int rows) {
   const bool lat_ok = kv.latent_dtype == MLA_BF16 || (kv.latent_dtype == MLA_FP8E4M3 && kv.scale);
   return q_dtype == MLA_BF16 && lat_ok && kv.rope_dtype == MLA_BF16 && kv.d_c == 512 &&
-         kv.d_r == 64 && kv.block_size == kTok && h >= 1 && h <= 128 && tc_device();
+         kv.d_r == 64 && kv.block_size == kTok && rows >= 1 && tc_device();
 }
 
 namespace {
@@ -1337,7 +1352,7 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_
 
 template <bool kFp8>
 cudaError_t launch_variant(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope,
-                           const CUtensorMap& tm_q, const TcParams& prm, int num_parts,
+                           const CUtensorMap& tm_q, const TcParams& prm, int num_pairs,
                            cudaStream_t s) {
   // the dynamic shared-memory limit is a per-device setting: once per device
   int dev = 0;
@@ -1349,7 +1364,7 @@ cudaError_t launch_variant(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope
                                      Cfg<kFp8>::kSmemAlloc);
   });
   if (r != 0) return r < 0 ? cudaErrorInvalidDevice : (cudaError_t)r;
-  dim3 grid(2 * num_parts);
+  dim3 grid(2 * num_pairs);
   decode_tc_kernel<kFp8><<<grid, Cfg<kFp8>::kThreads, Cfg<kFp8>::kSmemAlloc, s>>>(tm_lat, tm_rope,
                                                                                  tm_q, prm);
   return cudaGetLastError();
@@ -1359,9 +1374,11 @@ cudaError_t launch_variant(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope
 
 cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
-                             int B, int h, int num_parts, float scale, float* o_part,
-                             float* lse_part, int32_t* status, bool test_timeout,
+                             int B, int q_len, int heads, int num_parts, float scale,
+                             float* o_part, float* lse_part, int32_t* status, bool test_timeout,
                              cudaStream_t s) {
+  const int h = q_len * heads;                 // query rows per sequence
+  const int groups = (h + 127) / 128;          // CTA pairs per part
   const bool fp8 = kv.latent_dtype == MLA_FP8E4M3;
   CUtensorMap tm_lat, tm_rope, tm_q;
   const uint64_t rows = (uint64_t)kv.num_blocks * kv.block_size;
@@ -1382,13 +1399,15 @@ cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
   prm.max_blocks = max_blocks;
   prm.B = B;
   prm.h = h;
+  prm.heads = heads;
+  prm.q_len = q_len;
   prm.num_parts = num_parts;
   prm.num_blocks = kv.num_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.wait_limit = 4000000000LL;  // about 2 s of SM clock
   prm.test_wait_limit = test_timeout ? 20000 : 0;  // about 10 us
-  return fp8 ? launch_variant<true>(tm_lat, tm_rope, tm_q, prm, num_parts, s)
-             : launch_variant<false>(tm_lat, tm_rope, tm_q, prm, num_parts, s);
+  return fp8 ? launch_variant<true>(tm_lat, tm_rope, tm_q, prm, num_parts * groups, s)
+             : launch_variant<false>(tm_lat, tm_rope, tm_q, prm, num_parts * groups, s);
 }
 
 }  // namespace mla

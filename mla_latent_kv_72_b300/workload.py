@@ -30,7 +30,7 @@ class DeviceWorkload:
 
     def __init__(self, w: mi.Workload, device="cuda", num_parts: int | None = None,
                  rows_per_upload: int = 1 << 20, out_dtype=torch.float32,
-                 fill_lens: np.ndarray | None = None):
+                 fill_lens: np.ndarray | None = None, q_len: int = 1):
         self.w = w
         self.device = torch.device(device)
         dev = self.device
@@ -45,13 +45,21 @@ class DeviceWorkload:
         self.max_len = int(lens.max())
         tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
 
-        qn, qr = mi.queries(w)
+        # q_len new tokens per sequence: queries [B, q_len, h, .] at positions
+        # L_b - q_len + j (q_len = 1 keeps the one-token shapes [B, h, .])
+        self.q_len = int(q_len)
+        if self.q_len == 1:
+            qn, qr = mi.queries(w)
+        else:
+            qn, qr = mi.queries_multi(w, self.q_len)
         wuk, wuv = mi.weights(w)
         self.q_nope = storage_to_torch(qn, w.dtype, dev)
         self.q_rope = storage_to_torch(qr, w.dtype, dev)
         self.w_uk = storage_to_torch(wuk, w.dtype, dev)
         self.w_uv = storage_to_torch(wuv, w.dtype, dev)
-        self.q_pos = torch.from_numpy(mi.query_positions(w, lens)).to(dev)
+        self.q_pos = torch.from_numpy(
+            mi.query_positions(w, lens) if self.q_len == 1 else
+            mi.query_positions_multi(w, self.q_len, lens)).to(dev)
         self.seq_lens = torch.from_numpy(lens.astype(np.int32)).to(dev)
         self.block_table = torch.from_numpy(table).to(dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -74,12 +82,14 @@ class DeviceWorkload:
         self.num_parts = int(num_parts)
         B, h = w.B, w.h
         nslot = C.mla_decode_num_partials(B, self.num_parts)
-        self.q_cat = torch.empty((B, h, d_c + d_r), dtype=tdt, device=dev)
-        self.o_part = torch.empty((nslot, h, d_c), dtype=torch.float32, device=dev)
-        self.lse_part = torch.empty((nslot, h), dtype=torch.float32, device=dev)
-        self.o_lat = torch.empty((B, h, d_c), dtype=tdt, device=dev)
-        self.lse = torch.empty((B, h), dtype=torch.float32, device=dev)
-        self.out = torch.empty((B, h, w.d_v), dtype=out_dtype, device=dev)
+        lead = (B,) if self.q_len == 1 else (B, self.q_len)
+        rows = self.q_len * h
+        self.q_cat = torch.empty(lead + (h, d_c + d_r), dtype=tdt, device=dev)
+        self.o_part = torch.empty((nslot, rows, d_c), dtype=torch.float32, device=dev)
+        self.lse_part = torch.empty((nslot, rows), dtype=torch.float32, device=dev)
+        self.o_lat = torch.empty(lead + (h, d_c), dtype=tdt, device=dev)
+        self.lse = torch.empty(lead + (h,), dtype=torch.float32, device=dev)
+        self.out = torch.empty(lead + (h, w.d_v), dtype=out_dtype, device=dev)
 
     # -- cache -------------------------------------------------------------
     def _fill(self, rows_per_upload: int) -> None:
@@ -136,22 +146,32 @@ class DeviceWorkload:
         return calls
 
     # -- the decode step ---------------------------------------------------
+    def _rows(self, t: torch.Tensor) -> torch.Tensor:
+        """[B, q_len, h, .] -> [B * q_len, h, .] (the per-token calls' view)."""
+        return t if self.q_len == 1 else t.reshape((-1,) + tuple(t.shape[2:]))
+
     def absorb(self, stream=None):
-        C.mla_absorb_q(self.q_nope, self.q_rope, self.q_pos, self.w_uk, self.q_cat,
-                       rope_theta=self.w.theta, stream=stream)
+        C.mla_absorb_q(self._rows(self.q_nope), self._rows(self.q_rope), self.q_pos.reshape(-1),
+                       self.w_uk, self._rows(self.q_cat), rope_theta=self.w.theta, stream=stream)
 
     def attend(self, flags=C.MLA_DECODE_AUTO, stream=None):
-        C.mla_decode_fwd(self.q_cat, self.kv, self.block_table, self.seq_lens, self.num_parts,
-                         self.o_part, self.lse_part, dev_status=self.status, flags=flags,
-                         stream=stream)
+        if self.q_len == 1:
+            C.mla_decode_fwd(self.q_cat, self.kv, self.block_table, self.seq_lens,
+                             self.num_parts, self.o_part, self.lse_part, dev_status=self.status,
+                             flags=flags, stream=stream)
+        else:
+            C.mla_decode_fwd_multi(self.q_cat, self.kv, self.block_table, self.seq_lens,
+                                   self.num_parts, self.o_part, self.lse_part,
+                                   dev_status=self.status, flags=flags, stream=stream)
 
     def combine(self, stream=None):
+        B = self.w.B
         C.mla_combine(self.o_part, self.lse_part, self.seq_lens, self.w.block_size,
-                      self.block_table.shape[1], self.num_parts, self.o_lat, self.lse,
-                      stream=stream)
+                      self.block_table.shape[1], self.num_parts,
+                      self.o_lat.view(B, -1, self.w.d_c), self.lse.view(B, -1), stream=stream)
 
     def project(self, stream=None):
-        C.mla_out_proj(self.o_lat, self.w_uv, self.out, stream=stream)
+        C.mla_out_proj(self._rows(self.o_lat), self.w_uv, self._rows(self.out), stream=stream)
 
     def step(self, flags=C.MLA_DECODE_AUTO, stream=None):
         self.absorb(stream)
@@ -174,10 +194,10 @@ class DeviceWorkload:
         w = self.w
         el = 4 if w.dtype == "f32" else 2
         B, h = w.B, w.h
-        q_in = B * h * (w.d_nope + w.d_r) * el
+        q_in = B * self.q_len * h * (w.d_nope + w.d_r) * el
         wts = 2 * h * w.d_v * w.d_c * el
         table = self.table_np.size * 4 + B * 4
-        out = B * h * w.d_v * self.out.element_size()
+        out = B * self.q_len * h * w.d_v * self.out.element_size()
         return self.cache_bytes() + q_in + wts + table + out
 
     def decode_bytes(self) -> float:
@@ -185,19 +205,20 @@ class DeviceWorkload:
         once, the absorbed queries, the block table and the lengths."""
         w = self.w
         el = 4 if w.dtype == "f32" else 2
-        return (self.cache_bytes() + w.B * w.h * (w.d_c + w.d_r) * el
+        return (self.cache_bytes() + w.B * self.q_len * w.h * (w.d_c + w.d_r) * el
                 + self.table_np.size * 4 + w.B * 4)
 
     def decode_flops(self) -> float:
-        """2 * h * (d_c + d_r) score flops plus 2 * h * d_c P.C flops per cached token."""
+        """2 * h * (d_c + d_r) score flops plus 2 * h * d_c P.C flops per cached token
+        and query token (the masked corner of the causal triangle is not removed)."""
         w = self.w
-        return float(self.lens_np.sum()) * w.h * 2 * (w.d_c + w.d_r + w.d_c)
+        return float(self.lens_np.sum()) * self.q_len * w.h * 2 * (w.d_c + w.d_r + w.d_c)
 
     def step_flops(self) -> float:
         """2 * h * (d_c + d_r + d_c) per cached token, plus the two per-head GEMMs."""
         w = self.w
-        attn = float(self.lens_np.sum()) * w.h * 2 * (w.d_c + w.d_r + w.d_c)
-        gemms = 2.0 * w.B * w.h * w.d_c * (w.d_nope + w.d_v)
+        attn = float(self.lens_np.sum()) * self.q_len * w.h * 2 * (w.d_c + w.d_r + w.d_c)
+        gemms = 2.0 * w.B * self.q_len * w.h * w.d_c * (w.d_nope + w.d_v)
         return attn + gemms
 
     def check_status(self) -> int:

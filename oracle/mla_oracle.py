@@ -143,6 +143,42 @@ def decode_reference(q_nope, q_rope, q_pos, w_uk, w_uv, seqs, *, heads=None,
     return {"out": out, "o_lat": o_lat, "lse": lse}
 
 
+def decode_reference_multi(q_nope, q_rope, w_uk, w_uv, seqs, *, heads=None, scale=None,
+                           theta=ROPE_THETA):
+    """Non-absorbed MLA decode of q_len new tokens per sequence (multi-token
+    prediction or speculative decoding verify several tokens in one step).
+
+    The L_b cached rows of sequence b include its q_len new tokens, so token j
+    sits at position L_b - q_len + j and, as in the MHA equation of kexue.fm
+    (keys i <= t), attends to the cached rows 0 .. L_b - q_len + j.  Token j's
+    output is ``decode_reference`` of its own query over those rows.
+
+    q_nope [B, q_len, h, d_nope], q_rope [B, q_len, h, d_r] (unrotated),
+    seqs as in ``decode_reference``.  Returns out [B, q_len, H, d_v],
+    o_lat [B, q_len, H, d_c], lse [B, q_len, H]; a token that sees no row
+    (L_b - q_len + j < 0) gets out = o_lat = 0 and lse = -inf.
+    """
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    q_rope = np.asarray(q_rope, dtype=np.float64)
+    B, q_len, h = q_nope.shape[:3]
+    H = h if heads is None else len(heads)
+    d_v, d_c = np.asarray(w_uv).shape[1], np.asarray(w_uk).shape[2]
+    out = np.zeros((B, q_len, H, d_v))
+    o_lat = np.zeros((B, q_len, H, d_c))
+    lse = np.full((B, q_len, H), -np.inf)
+    for b in range(B):
+        c, kr = seqs[b]
+        L = np.asarray(c).shape[0]
+        for j in range(q_len):
+            n = L - q_len + j + 1          # rows visible to token j
+            if n <= 0:
+                continue
+            r = decode_reference(q_nope[b:b + 1, j], q_rope[b:b + 1, j], [n - 1], w_uk, w_uv,
+                                 [(c[:n], kr[:n])], heads=heads, scale=scale, theta=theta)
+            out[b, j], o_lat[b, j], lse[b, j] = r["out"][0], r["o_lat"][0], r["lse"][0]
+    return {"out": out, "o_lat": o_lat, "lse": lse}
+
+
 def decode_absorbed(q_nope, q_rope, q_pos, w_uk, w_uv, seqs, *, heads=None,
                     scale=None, theta=ROPE_THETA):
     """Absorbed (MQA-form) MLA decode in float64.

@@ -491,3 +491,64 @@ def test_cache_append_reports_bad_positions():
     torch.cuda.synchronize()
     assert dw.check_status() == C.MLA_DEV_BAD_LENGTH
     assert torch.equal(dw.pool.view(torch.int16), before.view(torch.int16))   # nothing written
+
+
+# ----------------------------------------------------------------------------
+# multi-token decode (q_len new tokens per sequence, causal among them)
+# ----------------------------------------------------------------------------
+
+MULTI_CASES = {
+    # 64 rows (one CTA pair per part); lengths below q_len, at and around block edges
+    "h16_q4_edges": (mi.scaled(mi.workload(3), B=9, h=16, L=None,
+                               lens=(1, 2, 3, 63, 64, 65, 66, 67, 300)), 4),
+    # 256 rows: two row groups per part
+    "h128_q2": (mi.scaled(mi.workload(4), B=3, L_range=(60, 400)), 2),
+    # FP8 latent, 384 rows: three row groups
+    "fp8_h128_q3": (mi.scaled(mi.workload(5), B=2, L=None, lens=(130, 259)), 3),
+}
+
+
+def check_multi(w, q_len, dw, tol):
+    inp = O.workload_inputs_f64(w)
+    qn, qr = mi.queries_multi(w, q_len)
+    seqs = [O.sequence_view(w, b, int(inp["lens"][b])) for b in range(w.B)]
+    ref = O.decode_reference_multi(mi.storage_to_f64(qn, w.dtype), mi.storage_to_f64(qr, w.dtype),
+                                   inp["w_uk"], inp["w_uv"], seqs)
+    out = dw.out.float().cpu().numpy()
+    o_lat = dw.o_lat.float().cpu().numpy()
+    lse = dw.lse.float().cpu().numpy()
+    # tokens that see no row: output 0 and lse -inf, as in the oracle
+    empty = np.isneginf(ref["lse"])
+    np.testing.assert_array_equal(np.isneginf(lse), empty)
+    assert np.all(out[empty] == 0) and np.all(o_lat[empty] == 0)
+    assert rel_err(out, ref["out"]) <= tol
+    assert rel_err(o_lat, ref["o_lat"]) <= tol
+    assert abs_err(lse[~empty], ref["lse"][~empty]) <= tol
+
+
+@pytest.mark.parametrize("flags", [0, 1], ids=["auto", "simt"])
+@pytest.mark.parametrize("name", list(MULTI_CASES))
+def test_multi_token_decode_matches_oracle(name, flags):
+    w, q_len = MULTI_CASES[name]
+    dw = make(w, q_len=q_len, num_parts=7)
+    dw.step(flags=flags)
+    torch.cuda.synchronize()
+    assert dw.check_status() == 0
+    check_multi(w, q_len, dw, TOL["bf16"])
+
+
+def test_multi_token_entry_with_one_token_equals_the_one_token_decode():
+    from mla_latent_kv_72_b300 import binding as C
+    w = mi.scaled(mi.workload(4), B=4, L_range=(1, 500))
+    dw = make(w, num_parts=9)
+    dw.absorb()
+    dw.attend()
+    torch.cuda.synchronize()
+    o2 = torch.full_like(dw.o_part, float("nan"))
+    l2 = torch.full_like(dw.lse_part, float("nan"))
+    C.mla_decode_fwd_multi(dw.q_cat.unsqueeze(1), dw.kv, dw.block_table, dw.seq_lens,
+                           dw.num_parts, o2, l2, dev_status=dw.status)
+    torch.cuda.synchronize()
+    slots = sorted(expected_slots(dw.lens_np, w.block_size, dw.num_parts))
+    assert torch.equal(o2[slots].view(torch.int32), dw.o_part[slots].view(torch.int32))
+    assert torch.equal(l2[slots].view(torch.int32), dw.lse_part[slots].view(torch.int32))

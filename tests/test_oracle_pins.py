@@ -612,3 +612,88 @@ def test_quantized_latent_appended_reduces_to_the_fill():
         blk, sc = O.fp8_append_row(blk, sc, x[r])
     np.testing.assert_array_equal(codes[64:128], blk)
     assert scales[1] == sc
+
+
+# ----------------------------------------------------------------------------
+# multi-token decode (q_len new tokens, causal among them)
+# ----------------------------------------------------------------------------
+
+def _brute_force_multi(qn, qr, wuk, wuv, seqs, theta=10000.0):
+    # scalar loops with an explicit causal mask: token j of sequence b is at
+    # position L - q_len + j and sees the rows at positions <= its own
+    B, q_len, h, d_nope = qn.shape
+    d_r = qr.shape[3]
+    d_v, d_c = wuv.shape[1], wuk.shape[2]
+    sc = 1.0 / math.sqrt(d_nope + d_r)
+    out = np.zeros((B, q_len, h, d_v))
+    for b in range(B):
+        c, kr = seqs[b]
+        L = len(c)
+        for j in range(q_len):
+            pos = L - q_len + j
+            for s in range(h):
+                z = []
+                for i in range(L):
+                    if i > pos:
+                        continue
+                    dot = 0.0
+                    for d in range(d_nope):
+                        kd = sum(c[i][cc] * wuk[s][d][cc] for cc in range(d_c))
+                        dot += qn[b][j][s][d] * kd
+                    for p2 in range(d_r // 2):
+                        a_q = pos * theta ** (-2.0 * p2 / d_r)
+                        a_k = i * theta ** (-2.0 * p2 / d_r)
+                        q0, q1 = qr[b][j][s][2 * p2], qr[b][j][s][2 * p2 + 1]
+                        k0, k1 = kr[i][2 * p2], kr[i][2 * p2 + 1]
+                        rq = (q0 * math.cos(a_q) - q1 * math.sin(a_q), q0 * math.sin(a_q) + q1 * math.cos(a_q))
+                        rk = (k0 * math.cos(a_k) - k1 * math.sin(a_k), k0 * math.sin(a_k) + k1 * math.cos(a_k))
+                        dot += rq[0] * rk[0] + rq[1] * rk[1]
+                    z.append((i, dot * sc))
+                if not z:
+                    continue
+                mz = max(v for _, v in z)
+                ws = [(i, math.exp(v - mz)) for i, v in z]
+                tot = sum(wv for _, wv in ws)
+                for v in range(d_v):
+                    out[b, j, s, v] = sum(wv * sum(c[i][cc] * wuv[s][v][cc] for cc in range(d_c))
+                                          for i, wv in ws) / tot
+    return out
+
+
+def test_multi_token_decode_bruteforce_and_mask():
+    rng = np.random.default_rng(41)
+    B, q_len, h, d_c, d_r, d_nope, d_v = 2, 3, 2, 6, 4, 3, 4
+    qn = rng.standard_normal((B, q_len, h, d_nope))
+    qr = rng.standard_normal((B, q_len, h, d_r))
+    wuk = rng.standard_normal((h, d_nope, d_c)) / math.sqrt(d_c)
+    wuv = rng.standard_normal((h, d_v, d_c)) / math.sqrt(d_c)
+    seqs = [(rng.standard_normal((L, d_c)), rng.standard_normal((L, d_r))) for L in (5, 2)]
+    ref = O.decode_reference_multi(qn, qr, wuk, wuv, seqs)
+    bf = _brute_force_multi(qn, qr, wuk, wuv, seqs)
+    np.testing.assert_allclose(ref["out"], bf, rtol=1e-12, atol=1e-14)
+    # sequence 1 has L = 2 < q_len: its first token sees nothing
+    assert np.all(ref["out"][1, 0] == 0) and np.all(np.isneginf(ref["lse"][1, 0]))
+    assert np.all(np.isfinite(ref["lse"][1, 1:]))
+
+
+def test_multi_token_decode_is_causal_and_reduces_to_one_token():
+    rng = np.random.default_rng(42)
+    qn, qr, _, wuk, wuv, seqs = _rand_case(rng, B=2, h=3, lens=(9, 7))
+    # q_len = 1 is the one-token decode at the last position
+    one = O.decode_reference_multi(qn[:, None], qr[:, None], wuk, wuv, seqs)
+    ref = O.decode_reference(qn, qr, [8, 6], wuk, wuv, seqs)
+    np.testing.assert_allclose(one["out"][:, 0], ref["out"], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(one["lse"][:, 0], ref["lse"], rtol=1e-13)
+    # token j never sees the rows after its own position: changing them only
+    # changes the later tokens
+    q4n = rng.standard_normal((2, 4, 3, qn.shape[2]))
+    q4r = rng.standard_normal((2, 4, 3, qr.shape[2]))
+    a = O.decode_reference_multi(q4n, q4r, wuk, wuv, seqs)
+    seqs2 = [(c.copy(), k.copy()) for c, k in seqs]
+    seqs2[0][0][-1] += 5.0         # the last row (position 8: token 3 only)
+    seqs2[1][1][-2] -= 3.0         # position 5 of L = 7: tokens 2 and 3
+    b = O.decode_reference_multi(q4n, q4r, wuk, wuv, seqs2)
+    np.testing.assert_array_equal(a["out"][0, :3], b["out"][0, :3])
+    assert not np.allclose(a["out"][0, 3], b["out"][0, 3])
+    np.testing.assert_array_equal(a["out"][1, :2], b["out"][1, :2])
+    assert not np.allclose(a["out"][1, 2:], b["out"][1, 2:])
