@@ -301,6 +301,40 @@ int mla_out_proj(const void* o_lat, const void* w_uv, void* out, int B, int h, i
                  int d_v, int in_dtype, int out_dtype, void* stream);
 
 /*
+ * The hidden-state boundary of the step: the query side starts from the
+ * hidden state x_t through the compressed query (kexue.fm "Part 3": the
+ * query is also low-rank, c'_t = x_t W_c', and each head's query is read off
+ * c'_t; iotdigitaltwinplm.com "Query compression is separate": the query's
+ * own down-projection is not cached), and the output side ends in the
+ * output projection W_O (kexue.fm "Part 1": W_v can be merged into the
+ * projection that follows o_t).  Those are plain linear layers:
+ *
+ * mla_linear: y[m, n] = sum_k x[m, k] w[n, k]   (w stored [N, K], as a
+ * linear layer's weight), bf16 x and w, float32 accumulation, y in y_dtype
+ * (MLA_F32 or MLA_BF16).  Supported: K % 64 == 0, N % 128 == 0.  Long
+ * contractions are split over CTAs; the float32 split partials go to the
+ * caller's workspace of mla_linear_workspace_bytes(M, K, N) bytes (0: none
+ * needed; then workspace may be NULL) and are summed in a fixed order, so
+ * results do not depend on timing.  A too small workspace is MLA_ERR_ARG.
+ */
+size_t mla_linear_workspace_bytes(int M, int K, int N);
+int mla_linear(const void* x, const void* w, void* y, int M, int K, int N, int y_dtype,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_fold_uv_into_o: merge W_UV into the output projection (kexue.fm "Part
+ * 1": the value up-projection moves into the projection after attention):
+ *   w_fold[n, s, c] = sum_v w_o[n, s * d_v + v] * w_uv[s, v, c]
+ *   w_uv [h, d_v, d_c], w_o [d_model, h * d_v], w_fold [d_model, h * d_c]: bf16
+ * so that y = o_lat . w_fold^T (mla_linear over the h * d_c latent outputs)
+ * equals (o_lat W_UV) W_O^T.  Supported: d_c = 512, d_v = 128.  The merged
+ * matrix holds d_c / d_v = 4 times the elements of W_O, so at decode, where
+ * weight reads bound these layers, the unmerged pair reads fewer bytes.
+ */
+int mla_fold_uv_into_o(const void* w_uv, const void* w_o, void* w_fold, int h, int d_c, int d_v,
+                       int d_model, void* stream);
+
+/*
  * mla_cache_fill: write whole sequences into the paged cache (the cache
  * content of iotdigitaltwinplm.com's listing, appended rows c_t and
  * RoPE(k_R, t); intvml.com: the RoPE key is cached in rotated form).

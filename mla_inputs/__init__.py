@@ -22,6 +22,8 @@ regenerated on its own):
   paged workload.
 * ``default_rng([seed, TAG_QM, q_len])``: queries of q_len new tokens per
   sequence (multi-token decode).
+* ``default_rng([seed, TAG_H, d_model, d_cq])``: the hidden state and the
+  linear layers around the step (query compression and output projection).
 
 All draws are float64; storage dtype "bf16" rounds f64 -> f32 -> bf16 with
 round-to-nearest-even at each step, "f32" rounds f64 -> f32.
@@ -39,6 +41,7 @@ TAG_W = 13
 TAG_L = 14
 TAG_P = 15
 TAG_QM = 16
+TAG_H = 17
 
 
 # ----------------------------------------------------------------------------
@@ -253,6 +256,21 @@ def weights(w: Workload) -> tuple[np.ndarray, np.ndarray]:
     wuk = rng.standard_normal((w.h, w.d_nope, w.d_c)) * s
     wuv = rng.standard_normal((w.h, w.d_v, w.d_c)) * s
     return to_storage(wuk, w.dtype), to_storage(wuv, w.dtype)
+
+
+def hidden_inputs(w: Workload, d_model: int, d_cq: int) -> dict:
+    """Storage form of the hidden-state side of a step: x [B, d_model] ~ N(0,1)
+    and the linear layers stored [out, in] with variance 1/fan_in: w_dq
+    [d_cq, d_model], w_uq [h * d_nope, d_cq], w_qr [h * d_r, d_cq], w_o
+    [d_model, h * d_v]."""
+    rng = np.random.default_rng([w.seed, TAG_H, d_model, d_cq])
+    x = rng.standard_normal((w.B, d_model))
+    wdq = rng.standard_normal((d_cq, d_model)) / math.sqrt(d_model)
+    wuq = rng.standard_normal((w.h * w.d_nope, d_cq)) / math.sqrt(d_cq)
+    wqr = rng.standard_normal((w.h * w.d_r, d_cq)) / math.sqrt(d_cq)
+    wo = rng.standard_normal((d_model, w.h * w.d_v)) / math.sqrt(w.h * w.d_v)
+    return {k: to_storage(v, w.dtype) for k, v in
+            {"x": x, "w_dq": wdq, "w_uq": wuq, "w_qr": wqr, "w_o": wo}.items()}
 
 
 def query_positions(w: Workload, lens: np.ndarray | None = None) -> np.ndarray:

@@ -26,6 +26,9 @@ from .binding import (  # noqa: F401
     mla_decode_attend_noalloc,
     default_num_parts,
     mla_out_proj,
+    mla_linear,
+    mla_linear_workspace_bytes,
+    mla_fold_uv_into_o,
     mla_paged_gather,
     mla_status_string,
     mla_version,

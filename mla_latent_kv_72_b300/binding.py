@@ -31,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_version", "mla_cache_bytes_per_token", "mla_absorb_q",
     "mla_decode_num_partials", "mla_decode_fwd", "mla_decode_fwd_multi", "mla_combine", "mla_decode_attend_noalloc",
     "mla_out_proj", "mla_cache_fill", "mla_cache_append", "mla_paged_gather",
+    "mla_linear_workspace_bytes", "mla_linear", "mla_fold_uv_into_o",
 )
 
 
@@ -112,6 +113,9 @@ def lib() -> ctypes.CDLL:
         "mla_out_proj": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
         "mla_cache_fill": (i32, [vp, vp, i32, vp, i32, i32, vp, i32, kvp, f64, vp, vp]),
         "mla_cache_append": (i32, [vp, vp, i32, vp, i32, vp, i32, kvp, f64, vp, vp]),
+        "mla_linear_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32]),
+        "mla_linear": (i32, [vp, vp, vp, i32, i32, i32, i32, vp, ctypes.c_size_t, vp]),
+        "mla_fold_uv_into_o": (i32, [vp, vp, vp, i32, i32, i32, i32, vp]),
         "mla_paged_gather": (i32, [kvp, vp, i32, vp, i32, i32, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -258,6 +262,30 @@ def mla_cache_append(c_new, k_rope_new, pos, block_table, kv: KVCache, rope_thet
         _ptr(c_new), _ptr(k_rope_new), dtype_code(c_new.dtype), _ptr(pos), B, _ptr(block_table),
         block_table.shape[1], ctypes.byref(kv), float(rope_theta), _ptr(dev_status),
         _stream(stream)))
+
+
+def mla_linear_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(lib().mla_linear_workspace_bytes(M, K, N))
+
+
+def mla_linear(x, w, y, workspace=None, stream=None):
+    """y[m, n] = sum_k x[m, k] w[n, k] (see mla72.h); x [M, K], w [N, K], y [M, N]."""
+    M, K = x.shape
+    N = w.shape[0]
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("mla_linear", lib().mla_linear(
+        _ptr(x), _ptr(w), _ptr(y), M, K, N, dtype_code(y.dtype), _ptr(workspace), ws,
+        _stream(stream)))
+    return y
+
+
+def mla_fold_uv_into_o(w_uv, w_o, w_fold, stream=None):
+    """w_fold [d_model, h * d_c] <- W_O merged with W_UV (see mla72.h)."""
+    h, d_v, d_c = w_uv.shape
+    d_model = w_o.shape[0]
+    _check("mla_fold_uv_into_o", lib().mla_fold_uv_into_o(
+        _ptr(w_uv), _ptr(w_o), _ptr(w_fold), h, d_c, d_v, d_model, _stream(stream)))
+    return w_fold
 
 
 def mla_paged_gather(kv: KVCache, block_table, cu_seqlens, max_len, latent_out=None,

@@ -179,6 +179,39 @@ int mla_out_proj(const void* o_lat, const void* w_uv, void* out, int B, int h, i
                                              out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
+size_t mla_linear_workspace_bytes(int M, int K, int N) {
+  if (M <= 0 || K <= 0 || N <= 0 || K % 64 != 0 || N % 128 != 0) return 0;
+  const int sp = mla::linear_splits(M, K, N);
+  return sp > 1 ? (size_t)sp * (size_t)M * (size_t)N * sizeof(float) : 0;
+}
+
+int mla_linear(const void* x, const void* w, void* y, int M, int K, int N, int y_dtype,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !w || !y) return MLA_ERR_ARG;
+  if (M <= 0 || K <= 0 || N <= 0) return MLA_ERR_ARG;
+  if (!is_float_dtype(y_dtype)) return MLA_ERR_DTYPE;
+  if (K % 64 != 0 || N % 128 != 0 || K > (1 << 20) || N > (1 << 20)) return MLA_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return MLA_ERR_ALIGN;
+  const size_t need = mla_linear_workspace_bytes(M, K, N);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return MLA_ERR_ARG;
+  if (need > 0 && !aligned16(workspace)) return MLA_ERR_ALIGN;
+  if (!mla::tc_device()) return MLA_ERR_DEVICE;
+  return from_cuda(mla::launch_linear_tc(x, w, y, M, K, N, y_dtype,
+                                         static_cast<float*>(workspace),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int mla_fold_uv_into_o(const void* w_uv, const void* w_o, void* w_fold, int h, int d_c, int d_v,
+                       int d_model, void* stream) {
+  if (!w_uv || !w_o || !w_fold) return MLA_ERR_ARG;
+  if (h <= 0 || d_c <= 0 || d_v <= 0 || d_model <= 0) return MLA_ERR_ARG;
+  if (d_c != 512 || d_v != 128) return MLA_ERR_SHAPE;
+  if (!aligned16(w_uv) || !aligned16(w_o) || !aligned16(w_fold)) return MLA_ERR_ALIGN;
+  if (!mla::tc_device()) return MLA_ERR_DEVICE;
+  return from_cuda(mla::launch_fold_uv_o_tc(w_uv, w_o, w_fold, h, d_model,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 int mla_cache_fill(const void* c_kv, const void* k_rope, int src_dtype,
                    const int32_t* cu_seqlens, int B, int max_len, const int32_t* block_table,
                    int max_blocks_per_seq, const mla_kv_cache* kv, double rope_theta,

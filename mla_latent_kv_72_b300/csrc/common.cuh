@@ -167,6 +167,15 @@ cudaError_t launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int
 cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, int B, int h,
                                int out_dtype, cudaStream_t s);
 
+// y[M, N] = x[M, K] W[N, K]^T (bf16 in, y_dtype out); part: float32 split
+// partials of linear_splits(M, K, N) * M * N floats when that is above 1
+int linear_splits(int M, int K, int N);
+cudaError_t launch_linear_tc(const void* x, const void* w, void* y, int M, int K, int N,
+                             int y_dtype, float* part, cudaStream_t s);
+// W_fold[n, s, c] = sum_v W_O[n, s * 128 + v] W_UV[s, v, c] (bf16)
+cudaError_t launch_fold_uv_o_tc(const void* w_uv, const void* w_o, void* w_fold, int h,
+                                int d_model, cudaStream_t s);
+
 cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                              int B, int q_len, int heads, int num_parts, float scale,

@@ -47,6 +47,10 @@ struct GemmParams {
   int stage_bytes;  // A chunk + X chunk, multiple of 1024
   int tmem_cols;    // power of two >= max(32, n_tile)
   int B, h;
+  // K-major A: the tile of (s, m tile mt, chunk kc) starts at row
+  // s * a_row_s + mt * 128, column s * a_col_s + kc * 64 of the 2-D A map
+  // (per-head weights: rows advance with s; split contraction: columns do)
+  int a_row_s, a_col_s;
   void* out;        // element (b, s, m) at out + (b * h + s) * out_ld + m
   int out_ld;
   int out_dtype;
@@ -116,7 +120,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         tma_load_2d(a_dst + kABytes / 2, &tm_a, mt * 128 + 64, s * p.K + kc * kKChunk, full(st));
       } else {
         // one box of 64 k (contiguous) x 128 m rows
-        tma_load_2d(a_dst, &tm_a, kc * kKChunk, s * 128 * gridDim.y + mt * 128, full(st));
+        tma_load_2d(a_dst, &tm_a, s * p.a_col_s + kc * kKChunk, s * p.a_row_s + mt * 128,
+                    full(st));
       }
       tma_load_3d(x_dst, &tm_x, kc * kKChunk, s, b0, full(st));
     }
@@ -222,6 +227,32 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 
 constexpr int kGSmemMax = kStagesG * (kABytes + kMaxN * kKChunk * 2) + 256 + 1024;
 
+// y[b, n] = sum_s part[b, s, n] over the split partials, in split order
+// (deterministic); four columns per thread.
+__global__ void __launch_bounds__(256)
+split_reduce_kernel(const float* __restrict__ part, int splits, int B, int N, void* y,
+                    int y_dtype) {
+  const int64_t i = ((int64_t)blockIdx.x * 256 + threadIdx.x) * 4;
+  if (i >= (int64_t)B * N) return;
+  const int b = (int)(i / N), n = (int)(i % N);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sp = 0; sp < splits; ++sp) {
+    const float4 v = *reinterpret_cast<const float4*>(part + ((int64_t)b * splits + sp) * N + n);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  if (y_dtype == MLA_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(y) + i) = acc;
+  } else {
+    uint2 pk;
+    pk.x = (uint32_t)f32_to_bf16_rn(acc.x) | ((uint32_t)f32_to_bf16_rn(acc.y) << 16);
+    pk.y = (uint32_t)f32_to_bf16_rn(acc.z) | ((uint32_t)f32_to_bf16_rn(acc.w) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + i) = pk;
+  }
+}
+
 // Pipeline shape for a contraction of K and a batch tile of n rows.
 void shape(GemmParams* p, int K, int n) {
   p->K = K;
@@ -323,6 +354,8 @@ cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, i
   shape(&p, 512, nt);
   p.B = B;
   p.h = h;
+  p.a_row_s = 128;
+  p.a_col_s = 0;
   p.out = out;
   p.out_ld = 128;
   p.out_dtype = out_dtype;
@@ -332,6 +365,93 @@ cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, i
   p.wait_limit = 4000000000LL;
   dim3 grid(h, 1, ceil_div(B, nt));
   head_gemm_kernel<false><<<grid, kGThreads, smem_bytes(p), s>>>(ta, tx, p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// plain linear layers and the W_UV / W_O fold
+// ---------------------------------------------------------------------------
+
+// Contraction splits of y = x W^T (M x K times N x K): enough CTAs to cover
+// the GPU about once (148 SMs on this part), each split at least 512 long.
+int linear_splits(int M, int K, int N) {
+  const int tiles = (N / 128) * ceil_div(M, n_tile_for(M));
+  int sp = 1;
+  while (sp < 64 && tiles * sp < 148 && (K / 64) % (2 * sp) == 0 && K / (2 * sp) >= 512) sp *= 2;
+  return sp;
+}
+
+cudaError_t launch_linear_tc(const void* x, const void* w, void* y, int M, int K, int N,
+                             int y_dtype, float* part, cudaStream_t s) {
+  const int sp = linear_splits(M, K, N);
+  const int ks = K / sp;
+  const int nt = n_tile_for(M);
+  // A: W as [N rows, K cols]; boxes of 64 k x 128 n
+  CUtensorMap ta, tx;
+  cuuint64_t adims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+  cuuint64_t astr[1] = {(cuuint64_t)K * 2};
+  cuuint32_t abox[2] = {64, 128};
+  // X: x as (k within split, split, row); boxes of 64 k x 1 x n_tile
+  cuuint64_t xdims[3] = {(cuuint64_t)ks, (cuuint64_t)sp, (cuuint64_t)M};
+  cuuint64_t xstr[2] = {(cuuint64_t)ks * 2, (cuuint64_t)K * 2};
+  cuuint32_t xbox[3] = {64, 1, (cuuint32_t)nt};
+  if (!encode(&ta, 2, w, adims, astr, abox) || !encode(&tx, 3, x, xdims, xstr, xbox))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr<false>();
+  if (e != cudaSuccess) return e;
+  GemmParams p{};
+  shape(&p, ks, nt);
+  p.B = M;
+  p.h = sp;
+  p.a_row_s = 0;
+  p.a_col_s = ks;
+  // one split: straight into y; several: float32 partials [M, splits, N]
+  p.out = sp == 1 ? y : static_cast<void*>(part);
+  p.out_ld = N;
+  p.out_dtype = sp == 1 ? y_dtype : MLA_F32;
+  p.q_rope = nullptr;
+  p.q_pos = nullptr;
+  p.status = nullptr;
+  p.wait_limit = 4000000000LL;
+  dim3 grid(sp, N / 128, ceil_div(M, nt));
+  head_gemm_kernel<false><<<grid, kGThreads, smem_bytes(p), s>>>(ta, tx, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || sp == 1) return e;
+  const int64_t n4 = (int64_t)M * N / 4;
+  split_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(part, sp, M, N, y, y_dtype);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fold_uv_o_tc(const void* w_uv, const void* w_o, void* w_fold, int h,
+                                int d_model, cudaStream_t s) {
+  // W_fold[n, s, c] = sum_v W_O[n, s * 128 + v] W_UV[s, v, c]: per head s,
+  // D[c][n] = sum_v A_s[c][v] X_s[n][v] with A_s[c][v] = W_UV[s][v][c]
+  // (MN-major, as W_UK in the absorbed query) and X_s[n][v] = W_O[n][s][v]
+  CUtensorMap ta, tx;
+  cuuint64_t adims[2] = {512, (cuuint64_t)h * 128};
+  cuuint64_t astr[1] = {512 * 2};
+  cuuint32_t abox[2] = {64, 64};
+  const int nt = n_tile_for(d_model);
+  cuuint64_t xdims[3] = {128, (cuuint64_t)h, (cuuint64_t)d_model};
+  cuuint64_t xstr[2] = {128 * 2, (cuuint64_t)h * 128 * 2};
+  cuuint32_t xbox[3] = {64, 1, (cuuint32_t)nt};
+  if (!encode(&ta, 2, w_uv, adims, astr, abox) || !encode(&tx, 3, w_o, xdims, xstr, xbox))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr<true>();
+  if (e != cudaSuccess) return e;
+  GemmParams p{};
+  shape(&p, 128, nt);
+  p.B = d_model;
+  p.h = h;
+  p.out = w_fold;
+  p.out_ld = 512;
+  p.out_dtype = MLA_BF16;
+  p.q_rope = nullptr;
+  p.q_pos = nullptr;
+  p.status = nullptr;
+  p.wait_limit = 4000000000LL;
+  dim3 grid(h, 512 / 128, ceil_div(d_model, nt));
+  head_gemm_kernel<true><<<grid, kGThreads, smem_bytes(p), s>>>(ta, tx, p);
   return cudaGetLastError();
 }
 

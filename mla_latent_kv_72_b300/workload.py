@@ -145,6 +145,61 @@ class DeviceWorkload:
         torch.cuda.synchronize(self.device)
         return calls
 
+    # -- the hidden-state boundary -----------------------------------------
+    def enable_hidden(self, d_model: int, d_cq: int) -> None:
+        """Upload the hidden state x and the linear layers around the step
+        (query compression W_DQ, W_UQ, W_QR; output projection W_O) and the
+        buffers of query_from_hidden / hidden_out."""
+        w = self.w
+        assert self.q_len == 1 and w.dtype == "bf16"
+        hid = mi.hidden_inputs(w, d_model, d_cq)
+        for k, v in hid.items():
+            setattr(self, k, storage_to_torch(v, w.dtype, self.device))
+        dev, B, h = self.device, w.B, w.h
+        self.d_model, self.d_cq = d_model, d_cq
+        self.c_q = torch.empty((B, d_cq), dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty((B, d_model), dtype=torch.float32, device=dev)
+        self.out_bf16 = torch.empty((B, h, w.d_v), dtype=torch.bfloat16, device=dev)
+        self.w_fold = None
+        ws = max(C.mla_linear_workspace_bytes(B, d_model, d_cq),
+                 C.mla_linear_workspace_bytes(B, d_cq, h * w.d_nope),
+                 C.mla_linear_workspace_bytes(B, d_cq, h * w.d_r),
+                 C.mla_linear_workspace_bytes(B, h * w.d_v, d_model),
+                 C.mla_linear_workspace_bytes(B, h * w.d_c, d_model))
+        self.lin_ws = torch.empty(max(1, ws // 4), dtype=torch.float32, device=dev)
+
+    def query_from_hidden(self, stream=None):
+        """q_nope, q_rope <- the compressed query of x (three linear layers)."""
+        w = self.w
+        B = w.B
+        C.mla_linear(self.x, self.w_dq, self.c_q, self.lin_ws, stream)
+        C.mla_linear(self.c_q, self.w_uq, self.q_nope.view(B, -1), self.lin_ws, stream)
+        C.mla_linear(self.c_q, self.w_qr, self.q_rope.view(B, -1), self.lin_ws, stream)
+
+    def hidden_out(self, folded: bool = False, stream=None):
+        """y <- the step's output projected to the hidden size: W_UV then W_O
+        (folded=False), or the merged W_O W_UV applied to o_lat (folded=True)."""
+        w = self.w
+        B = w.B
+        if folded:
+            if self.w_fold is None:
+                self.w_fold = torch.empty((self.d_model, w.h * w.d_c), dtype=torch.bfloat16,
+                                          device=self.device)
+                C.mla_fold_uv_into_o(self.w_uv, self.w_o, self.w_fold, stream)
+            C.mla_linear(self.o_lat.view(B, -1), self.w_fold, self.y, self.lin_ws, stream)
+        else:
+            C.mla_out_proj(self.o_lat, self.w_uv, self.out_bf16, stream=stream)
+            C.mla_linear(self.out_bf16.view(B, -1), self.w_o, self.y, self.lin_ws, stream)
+
+    def hidden_step(self, folded: bool = False, stream=None):
+        """The whole step from the hidden state x to the output hidden state y."""
+        self.query_from_hidden(stream)
+        self.absorb(stream)
+        self.attend(stream=stream)
+        self.combine(stream)
+        self.hidden_out(folded, stream)
+        return self.y
+
     # -- the decode step ---------------------------------------------------
     def _rows(self, t: torch.Tensor) -> torch.Tensor:
         """[B, q_len, h, .] -> [B * q_len, h, .] (the per-token calls' view)."""

@@ -230,6 +230,53 @@ def output_projection(o_lat, w_uv):
                      np.asarray(w_uv, dtype=np.float64))
 
 
+def query_from_hidden(x, w_dq, w_uq, w_qr, h):
+    """Per-head queries from the hidden state through the compressed query
+    (kexue.fm "Part 3": c'_t = x_t W_c'; every head's content query
+    c'_t W_qc^(s) and rotary query c'_t W_qr^(s) are read off it).
+
+    x [B, d_model]; weights stored [out, in] as linear layers: w_dq
+    [d_cq, d_model], w_uq [h * d_nope, d_cq], w_qr [h * d_r, d_cq].
+    Returns q_nope [B, h, d_nope] and the unrotated q_rope [B, h, d_r].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    c = x @ np.asarray(w_dq, dtype=np.float64).T
+    qn = c @ np.asarray(w_uq, dtype=np.float64).T
+    qr = c @ np.asarray(w_qr, dtype=np.float64).T
+    B = x.shape[0]
+    return qn.reshape(B, h, -1), qr.reshape(B, h, -1)
+
+
+def output_to_hidden(out, w_o):
+    """y_t = [o^(1), ..., o^(h)] W_O^T: the heads' value outputs [B, h, d_v]
+    concatenated and projected back to the hidden size (w_o [d_model, h * d_v])."""
+    out = np.asarray(out, dtype=np.float64)
+    return out.reshape(out.shape[0], -1) @ np.asarray(w_o, dtype=np.float64).T
+
+
+def fold_uv_into_o(w_uv, w_o):
+    """The output projection with W_UV merged in (kexue.fm "Part 1": W_v moves
+    into the projection after attention): w_fold[n, s * d_c + c] =
+    sum_v w_o[n, s * d_v + v] w_uv[s, v, c], so that y = o_lat w_fold^T."""
+    w_uv = np.asarray(w_uv, dtype=np.float64)
+    w_o = np.asarray(w_o, dtype=np.float64)
+    h, d_v, d_c = w_uv.shape
+    d_model = w_o.shape[0]
+    fold = np.einsum("nsv,svc->nsc", w_o.reshape(d_model, h, d_v), w_uv)
+    return fold.reshape(d_model, h * d_c)
+
+
+def decode_from_hidden(x, w_dq, w_uq, w_qr, w_uk, w_uv, w_o, q_pos, seqs, *, theta=ROPE_THETA):
+    """The whole decode step at the hidden-state boundary, non-absorbed:
+    queries from x (``query_from_hidden``), attention as ``decode_reference``,
+    output through W_UV and W_O (``output_to_hidden``).  Returns y [B, d_model]
+    and the intermediate dict of ``decode_reference``."""
+    h = np.asarray(w_uk).shape[0]
+    qn, qr = query_from_hidden(x, w_dq, w_uq, w_qr, h)
+    r = decode_reference(qn, qr, q_pos, w_uk, w_uv, seqs, theta=theta)
+    return output_to_hidden(r["out"], w_o), r
+
+
 def merge_partials(o_parts, lses):
     """Merge attention computed over disjoint key ranges.
 

@@ -552,3 +552,64 @@ def test_multi_token_entry_with_one_token_equals_the_one_token_decode():
     slots = sorted(expected_slots(dw.lens_np, w.block_size, dw.num_parts))
     assert torch.equal(o2[slots].view(torch.int32), dw.o_part[slots].view(torch.int32))
     assert torch.equal(l2[slots].view(torch.int32), dw.lse_part[slots].view(torch.int32))
+
+
+# ----------------------------------------------------------------------------
+# linear layers, the W_UV / W_O fold and the step at the hidden-state boundary
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,N", [(64, 7168, 1536), (5, 512, 256), (300, 1024, 384),
+                                   (64, 16384, 1024)])
+def test_linear_matches_float64(M, K, N):
+    from mla_latent_kv_72_b300 import binding as C
+    g = torch.Generator(device="cpu").manual_seed(M * 7 + N)
+    x = torch.randn((M, K), generator=g).to(torch.bfloat16)
+    wt = (torch.randn((N, K), generator=g) / K ** 0.5).to(torch.bfloat16)
+    ref = x.double() @ wt.double().T
+    ws_bytes = C.mla_linear_workspace_bytes(M, K, N)
+    ws = torch.empty(max(1, ws_bytes // 4), dtype=torch.float32, device="cuda")
+    xg, wg = x.cuda(), wt.cuda()
+    for dt, tol in ((torch.float32, 1e-5), (torch.bfloat16, 2.0 ** -8)):
+        y = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
+        C.mla_linear(xg, wg, y, ws)
+        torch.cuda.synchronize()
+        assert rel_err(y.double().cpu().numpy(), ref.numpy()) <= tol
+    # the same inputs give the same bits (fixed-order sum of the splits)
+    y2 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    y3 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    C.mla_linear(xg, wg, y2, ws)
+    C.mla_linear(xg, wg, y3, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y2.view(torch.int32), y3.view(torch.int32))
+
+
+def test_fold_matches_oracle():
+    from mla_latent_kv_72_b300 import binding as C
+    w = mi.scaled(mi.workload(3), B=2, h=16)
+    _, wuv = mi.weights(w)
+    hid = mi.hidden_inputs(w, 1024, 256)
+    from mla_latent_kv_72_b300.workload import storage_to_torch
+    wuv_t = storage_to_torch(wuv, "bf16", "cuda")
+    wo_t = storage_to_torch(hid["w_o"], "bf16", "cuda")
+    fold = torch.empty((1024, 16 * 512), dtype=torch.bfloat16, device="cuda")
+    C.mla_fold_uv_into_o(wuv_t, wo_t, fold)
+    torch.cuda.synchronize()
+    ref = O.fold_uv_into_o(mi.storage_to_f64(wuv, "bf16"), mi.storage_to_f64(hid["w_o"], "bf16"))
+    assert rel_err(fold.float().cpu().numpy(), ref) <= 2.0 ** -8
+
+
+@pytest.mark.parametrize("folded", [False, True], ids=["w_uv_then_w_o", "folded"])
+def test_step_from_hidden_state_matches_oracle(folded):
+    w = mi.scaled(mi.workload(4), B=5, h=16, L_range=(1, 600))
+    d_model, d_cq = 1024, 256
+    dw = make(w, num_parts=7)
+    dw.enable_hidden(d_model, d_cq)
+    y = dw.hidden_step(folded=folded)
+    torch.cuda.synchronize()
+    assert dw.check_status() == 0
+    inp = O.workload_inputs_f64(w)
+    hid = {k: mi.storage_to_f64(v, "bf16") for k, v in mi.hidden_inputs(w, d_model, d_cq).items()}
+    seqs = [O.sequence_view(w, b, int(inp["lens"][b])) for b in range(w.B)]
+    y_ref, _ = O.decode_from_hidden(hid["x"], hid["w_dq"], hid["w_uq"], hid["w_qr"], inp["w_uk"],
+                                    inp["w_uv"], hid["w_o"], inp["q_pos"], seqs)
+    assert rel_err(y.cpu().numpy(), y_ref) <= TOL["bf16"]

@@ -697,3 +697,72 @@ def test_multi_token_decode_is_causal_and_reduces_to_one_token():
     assert not np.allclose(a["out"][0, 3], b["out"][0, 3])
     np.testing.assert_array_equal(a["out"][1, :2], b["out"][1, :2])
     assert not np.allclose(a["out"][1, 2:], b["out"][1, 2:])
+
+
+# ----------------------------------------------------------------------------
+# the hidden-state boundary: query compression and the output projection
+# ----------------------------------------------------------------------------
+
+def test_query_from_hidden_scalar_loops():
+    rng = np.random.default_rng(51)
+    B, d_model, d_cq, h, d_nope, d_r = 2, 7, 5, 3, 2, 4
+    x = rng.standard_normal((B, d_model))
+    wdq = rng.standard_normal((d_cq, d_model))
+    wuq = rng.standard_normal((h * d_nope, d_cq))
+    wqr = rng.standard_normal((h * d_r, d_cq))
+    qn, qr = O.query_from_hidden(x, wdq, wuq, wqr, h)
+    assert qn.shape == (B, h, d_nope) and qr.shape == (B, h, d_r)
+    for b in range(B):
+        c = [sum(x[b, i] * wdq[j, i] for i in range(d_model)) for j in range(d_cq)]
+        for s in range(h):
+            for d in range(d_nope):
+                want = sum(c[j] * wuq[s * d_nope + d, j] for j in range(d_cq))
+                assert abs(qn[b, s, d] - want) <= 1e-12
+            for d in range(d_r):
+                want = sum(c[j] * wqr[s * d_r + d, j] for j in range(d_cq))
+                assert abs(qr[b, s, d] - want) <= 1e-12
+
+
+def test_folded_output_projection_equals_the_pair():
+    # associativity: (o_lat W_UV^(s)T) W_O^T == o_lat W_fold^T, and a scalar
+    # loop over the fold's definition
+    rng = np.random.default_rng(52)
+    B, h, d_c, d_v, d_model = 3, 4, 6, 5, 7
+    o_lat = rng.standard_normal((B, h, d_c))
+    wuv = rng.standard_normal((h, d_v, d_c))
+    wo = rng.standard_normal((d_model, h * d_v))
+    fold = O.fold_uv_into_o(wuv, wo)
+    y_pair = O.output_to_hidden(O.output_projection(o_lat, wuv), wo)
+    y_fold = o_lat.reshape(B, -1) @ fold.T
+    np.testing.assert_allclose(y_fold, y_pair, rtol=1e-12, atol=1e-12)
+    for n in range(d_model):
+        for s in range(h):
+            for c in range(d_c):
+                want = sum(wo[n, s * d_v + v] * wuv[s, v, c] for v in range(d_v))
+                assert abs(fold[n, s * d_c + c] - want) <= 1e-12
+    # output_to_hidden concatenates heads in order
+    out = rng.standard_normal((B, h, d_v))
+    y = O.output_to_hidden(out, wo)
+    for b in range(B):
+        for n in range(d_model):
+            want = sum(out[b, s, v] * wo[n, s * d_v + v] for s in range(h) for v in range(d_v))
+            assert abs(y[b, n] - want) <= 1e-12
+
+
+def test_decode_from_hidden_composes_the_steps():
+    rng = np.random.default_rng(53)
+    B, h, d_c, d_r, d_nope, d_v, d_model, d_cq = 2, 3, 8, 4, 3, 5, 9, 6
+    x = rng.standard_normal((B, d_model))
+    wdq = rng.standard_normal((d_cq, d_model)) / 3
+    wuq = rng.standard_normal((h * d_nope, d_cq)) / 3
+    wqr = rng.standard_normal((h * d_r, d_cq)) / 3
+    wuk = rng.standard_normal((h, d_nope, d_c)) / 3
+    wuv = rng.standard_normal((h, d_v, d_c)) / 3
+    wo = rng.standard_normal((d_model, h * d_v)) / 3
+    seqs = [(rng.standard_normal((L, d_c)), rng.standard_normal((L, d_r))) for L in (6, 4)]
+    y, r = O.decode_from_hidden(x, wdq, wuq, wqr, wuk, wuv, wo, [5, 3], seqs)
+    qn, qr = O.query_from_hidden(x, wdq, wuq, wqr, h)
+    bf = _brute_force(qn.tolist(), qr.tolist(), [5, 3], wuk.tolist(), wuv.tolist(),
+                      [(c.tolist(), k.tolist()) for c, k in seqs])
+    np.testing.assert_allclose(r["out"], bf, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(y, bf.reshape(B, -1) @ wo.T, rtol=1e-12, atol=1e-13)
