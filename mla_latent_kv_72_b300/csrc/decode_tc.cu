@@ -97,6 +97,8 @@ constexpr int kXChunks = 16;                // 16-byte chunks per row
 constexpr int kRecvBytes = 128 * kXChunks * 16;
 
 constexpr int kNumBars = 40;
+// FP8 variant: warps that widen the e4m3 codes of each tile to bf16
+constexpr int kConvWarps = 4;
 
 // Layout of one variant: the bf16 cache (4 stages) or the FP8 latent cache (3
 // bf16 stages filled by converter warps from 2 FP8 landing buffers).
@@ -104,9 +106,9 @@ template <bool kFp8>
 struct Cfg {
   static constexpr int kStages = kFp8 ? 3 : kMaxStages;
   static constexpr int kLand = kFp8 ? 2 : 0;
-  // bf16: one more warp issues the P.C MMAs (warp 2 + kSoftWarps); FP8: two converter warps
+  // bf16: one more warp issues the P.C MMAs (warp 2 + kSoftWarps); FP8: kConvWarps converter warps
   static constexpr bool kSplitMma = !kFp8;
-  static constexpr int kThreads = 64 + 32 * kSoftWarps + (kFp8 ? 64 : 32);
+  static constexpr int kThreads = 64 + 32 * kSoftWarps + (kFp8 ? 32 * kConvWarps : 32);
   static constexpr int kOffStages = 0;
   static constexpr int kOffLand = kOffStages + kStages * kStageBytes;
   static constexpr int kOffRecv = kOffLand + kLand * kLandBytes;
@@ -343,12 +345,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(BAR_KV_FULL + s), kFp8 ? 3 : 1);   // FP8: + the two converter warps
+      mbar_init(bar(BAR_KV_FULL + s), kFp8 ? 1 + kConvWarps : 1);   // FP8: + the converter warps
       mbar_init(bar(BAR_KV_EMPTY + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(BAR_LAND_FULL + i), 1);
-      mbar_init(bar(BAR_LAND_EMPTY + i), 2);
+      mbar_init(bar(BAR_LAND_EMPTY + i), kConvWarps);
     }
     mbar_init(bar(BAR_S_EMPTY), kGroupWarps);
     for (int i = 0; i < kGroups; ++i) {
@@ -812,16 +814,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
     // bf16(e4m3 value x block scale) in the 128-byte-swizzled bf16 boxes of
     // stage st, where the MMAs read it (kexue.fm / iotdigitaltwinplm: the
     // latent is stored in FP8; one float32 scale per 64-token block).
-    const int ct = threadIdx.x - 32 * (2 + kSoftWarps);  // 0..63
+    const int ct = threadIdx.x - 32 * (2 + kSoftWarps);  // 0 .. 32 kConvWarps - 1
     const volatile int* land_pb = reinterpret_cast<const volatile int*>(smem + kOffMisc + 32);
     bool ok = true;
     for (int k = 0; k < ntiles; ++k) {
       const int j = k % 2, st = k % kStages;
       if (!warp_wait(bar(BAR_LAND_FULL + j), (k / 2) & 1)) { ok = false; break; }
+      if (ct == 0) MLA_TR(k, 22);
       const float sc = p.kv_scale[land_pb[j]];
       const uint8_t* src = smem + kOffLand + j * kLandBytes;
       uint8_t* dst = smem + kOffStages + st * kStageBytes;
-      for (int i = ct; i < 64 * 16; i += 64) {
+      const f2_t sc2 = f2_make(sc, sc);
+#pragma unroll 2
+      for (int i = ct; i < 64 * 16; i += 32 * kConvWarps) {
         const int r = i >> 4, q = i & 15;           // token row, 16-code group
         const uint4 v = *reinterpret_cast<const uint4*>(src + r * 256 + q * 16);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -833,7 +838,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
             const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
                 static_cast<__nv_fp8x2_storage_t>((w[e] >> (16 * hh)) & 0xFFFFu), __NV_E4M3);
             const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-            o[2 * e + hh] = pack_bf16x2(f.x * sc, f.y * sc);
+            float x0, x1;
+            f2_split(f2_mul(f2_make(f.x, f.y), sc2), x0, x1);
+            o[2 * e + hh] = pack_bf16x2(x0, x1);
           }
         }
         // codes 16q .. 16q+15 = latent columns of box q / 4, chunks 2 (q % 4) and +1
@@ -845,6 +852,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
+        MLA_TRMAX(k, 23);
         mbar_arrive(bar(BAR_LAND_EMPTY + j));
         mbar_arrive(bar(BAR_KV_FULL + st));
       }
