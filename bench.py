@@ -367,6 +367,9 @@ def run_ours(args) -> None:
     barrier()
     C.lib()
     w = resolve_workload(args.workload)
+    if args.batch is not None:
+        import mla_inputs as mi
+        w = mi.scaled(w, B=args.batch)
     parts = args.parts
     if parts is None and args.q_len > 1:
         # one CTA pair per part and per 128 query rows: keep one wave of pairs
@@ -581,6 +584,9 @@ def main(argv=None) -> None:
                    help="workload index 1..5 or name (default: the V3-shaped workload, 3)")
     p.add_argument("--parts", type=int, default=None,
                    help="balanced parts of the block stream (default: half the SM count)")
+    p.add_argument("--batch", type=int, default=None,
+                   help="sequences of the workload (default: its own B; a smaller B makes a "
+                        "profiling case of the same kernel)")
     p.add_argument("--q-len", type=int, default=1,
                    help="new tokens per sequence (multi-token decode; 1 = the one-token step)")
     p.add_argument("--settle-s", type=float, default=0.5,
