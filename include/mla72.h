@@ -335,6 +335,38 @@ int mla_fold_uv_into_o(const void* w_uv, const void* w_o, void* w_fold, int h, i
                        int d_model, void* stream);
 
 /*
+ * Prefill in the MHA form (kexue.fm "Part 3", eq. mla-mha, the form used for
+ * training and prefill; iotdigitaltwinplm.com "Prefill versus decode": the
+ * prompt's per-head keys and values are formed once and attention is
+ * compute-bound).  For every head s the key of token i is
+ * [c_i W_UK^(s), RoPE(k_R,i, i)] (192 values) and its value c_i W_UV^(s)
+ * (128 values); token t of a sequence attends to its tokens i <= t with
+ * the query [q_nope,t, RoPE(q_R,t, t)] and the scale 1/sqrt(192).  The
+ * sequences are packed: sequence b's tokens are rows cu_seqlens[b] ..
+ * cu_seqlens[b+1] - 1 (device int32 array of B + 1 entries), positions
+ * 0 .. L_b - 1, T = cu_seqlens[B] = total_rows rows in all.
+ *
+ * mla_prefill_query: q[t, s, 0:128] = q_nope[t, s, :] and
+ *   q[t, s, 128 + j] = RoPE(q_rope[t, s, :], position of t)[j] (angles in
+ *   float64, as mla_absorb_q).  q_nope [T, h, 128], q_rope [T, h, 64],
+ *   q [T, h, 192]: bf16.
+ * mla_prefill_fwd: out[t, s, :] = sum_{i <= t} p_ti v_i^(s), p the causal
+ *   softmax of the scores, lse[t, s] its natural-log denominator (lse may be
+ *   NULL).  q [T, h, 192] (from mla_prefill_query), k_nope [T, h, 128]
+ *   (= c W_UK^T: mla_linear of c with W_UK viewed [h * 128, 512]),
+ *   k_rope [T, 64] (the rotated RoPE key, shared by the heads: the cache's
+ *   rope rows), v [T, h, 128] (= c W_UV^T), all bf16; out [T, h, 128] in
+ *   out_dtype (MLA_F32 or MLA_BF16).  softmax_scale <= 0 selects 1/sqrt(192).
+ *   max_len bounds every L_b (it sizes the launch).
+ */
+int mla_prefill_query(const void* q_nope, const void* q_rope, const int32_t* cu_seqlens, int B,
+                      int max_len, int h, double rope_theta, void* q, void* stream);
+int mla_prefill_fwd(const void* q, const void* k_nope, const void* k_rope, const void* v,
+                    const int32_t* cu_seqlens, int B, int max_len, int64_t total_rows, int h,
+                    float softmax_scale, void* out, int out_dtype, float* lse,
+                    int32_t* dev_status, void* stream);
+
+/*
  * mla_cache_fill: write whole sequences into the paged cache (the cache
  * content of iotdigitaltwinplm.com's listing, appended rows c_t and
  * RoPE(k_R, t); intvml.com: the RoPE key is cached in rotated form).

@@ -24,6 +24,7 @@ regenerated on its own):
   sequence (multi-token decode).
 * ``default_rng([seed, TAG_H, d_model, d_cq])``: the hidden state and the
   linear layers around the step (query compression and output projection).
+* ``default_rng([seed, TAG_PF, b])``: the prompt queries of sequence b (prefill).
 
 All draws are float64; storage dtype "bf16" rounds f64 -> f32 -> bf16 with
 round-to-nearest-even at each step, "f32" rounds f64 -> f32.
@@ -42,6 +43,7 @@ TAG_L = 14
 TAG_P = 15
 TAG_QM = 16
 TAG_H = 17
+TAG_PF = 18
 
 
 # ----------------------------------------------------------------------------
@@ -256,6 +258,19 @@ def weights(w: Workload) -> tuple[np.ndarray, np.ndarray]:
     wuk = rng.standard_normal((w.h, w.d_nope, w.d_c)) * s
     wuv = rng.standard_normal((w.h, w.d_v, w.d_c)) * s
     return to_storage(wuk, w.dtype), to_storage(wuv, w.dtype)
+
+
+def prefill_queries(w: Workload, lens: np.ndarray | None = None) -> tuple[np.ndarray, np.ndarray]:
+    """Storage form of the prompt's queries, packed by sequence: q_nope
+    [T, h, d_nope] and unrotated q_rope [T, h, d_r], T = sum of the lengths,
+    standard normal (one stream per sequence)."""
+    lens = lengths(w) if lens is None else lens
+    qn, qr = [], []
+    for b, L in enumerate(lens):
+        rng = np.random.default_rng([w.seed, TAG_PF, b])
+        qn.append(rng.standard_normal((int(L), w.h, w.d_nope)))
+        qr.append(rng.standard_normal((int(L), w.h, w.d_r)))
+    return to_storage(np.concatenate(qn), w.dtype), to_storage(np.concatenate(qr), w.dtype)
 
 
 def hidden_inputs(w: Workload, d_model: int, d_cq: int) -> dict:

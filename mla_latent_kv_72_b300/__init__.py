@@ -30,6 +30,8 @@ from .binding import (  # noqa: F401
     mla_linear_workspace_bytes,
     mla_fold_uv_into_o,
     mla_paged_gather,
+    mla_prefill_fwd,
+    mla_prefill_query,
     mla_status_string,
     mla_version,
     EXPORTED_SYMBOLS,

@@ -31,7 +31,8 @@ EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_version", "mla_cache_bytes_per_token", "mla_absorb_q",
     "mla_decode_num_partials", "mla_decode_fwd", "mla_decode_fwd_multi", "mla_combine", "mla_decode_attend_noalloc",
     "mla_out_proj", "mla_cache_fill", "mla_cache_append", "mla_paged_gather",
-    "mla_linear_workspace_bytes", "mla_linear", "mla_fold_uv_into_o",
+    "mla_linear_workspace_bytes", "mla_linear", "mla_fold_uv_into_o", "mla_prefill_query",
+    "mla_prefill_fwd",
 )
 
 
@@ -116,6 +117,9 @@ def lib() -> ctypes.CDLL:
         "mla_linear_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32]),
         "mla_linear": (i32, [vp, vp, vp, i32, i32, i32, i32, vp, ctypes.c_size_t, vp]),
         "mla_fold_uv_into_o": (i32, [vp, vp, vp, i32, i32, i32, i32, vp]),
+        "mla_prefill_query": (i32, [vp, vp, vp, i32, i32, i32, f64, vp, vp]),
+        "mla_prefill_fwd": (i32, [vp, vp, vp, vp, vp, i32, i32, i64, i32, f32, vp, i32, vp, vp,
+                                  vp]),
         "mla_paged_gather": (i32, [kvp, vp, i32, vp, i32, i32, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -286,6 +290,28 @@ def mla_fold_uv_into_o(w_uv, w_o, w_fold, stream=None):
     _check("mla_fold_uv_into_o", lib().mla_fold_uv_into_o(
         _ptr(w_uv), _ptr(w_o), _ptr(w_fold), h, d_c, d_v, d_model, _stream(stream)))
     return w_fold
+
+
+def mla_prefill_query(q_nope, q_rope, cu_seqlens, max_len, q, rope_theta=10000.0, stream=None):
+    """q [T, h, 192] <- [q_nope, RoPE(q_rope) at each token's position] (see mla72.h)."""
+    B = cu_seqlens.shape[0] - 1
+    h = q_nope.shape[1]
+    _check("mla_prefill_query", lib().mla_prefill_query(
+        _ptr(q_nope), _ptr(q_rope), _ptr(cu_seqlens), B, int(max_len), h, float(rope_theta),
+        _ptr(q), _stream(stream)))
+    return q
+
+
+def mla_prefill_fwd(q, k_nope, k_rope, v, cu_seqlens, max_len, out, lse=None, *,
+                    softmax_scale=0.0, dev_status=None, stream=None):
+    """Causal prefill attention in the MHA form; out [T, h, 128] (see mla72.h)."""
+    B = cu_seqlens.shape[0] - 1
+    T, h, _ = q.shape
+    _check("mla_prefill_fwd", lib().mla_prefill_fwd(
+        _ptr(q), _ptr(k_nope), _ptr(k_rope), _ptr(v), _ptr(cu_seqlens), B, int(max_len), T, h,
+        float(softmax_scale), _ptr(out), dtype_code(out.dtype), _ptr(lse), _ptr(dev_status),
+        _stream(stream)))
+    return out
 
 
 def mla_paged_gather(kv: KVCache, block_table, cu_seqlens, max_len, latent_out=None,

@@ -212,6 +212,35 @@ int mla_fold_uv_into_o(const void* w_uv, const void* w_o, void* w_fold, int h, i
                                             static_cast<cudaStream_t>(stream)));
 }
 
+int mla_prefill_query(const void* q_nope, const void* q_rope, const int32_t* cu_seqlens, int B,
+                      int max_len, int h, double rope_theta, void* q, void* stream) {
+  if (!q_nope || !q_rope || !cu_seqlens || !q) return MLA_ERR_ARG;
+  if (B <= 0 || max_len < 0 || h <= 0 || !(rope_theta > 0.0)) return MLA_ERR_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(q)) return MLA_ERR_ALIGN;
+  if (max_len == 0) return MLA_OK;
+  return from_cuda(mla::launch_prefill_query(q_nope, q_rope, cu_seqlens, B, max_len, h,
+                                             rope_theta, q, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_prefill_fwd(const void* q, const void* k_nope, const void* k_rope, const void* v,
+                    const int32_t* cu_seqlens, int B, int max_len, int64_t total_rows, int h,
+                    float softmax_scale, void* out, int out_dtype, float* lse,
+                    int32_t* dev_status, void* stream) {
+  if (!q || !k_nope || !k_rope || !v || !cu_seqlens || !out) return MLA_ERR_ARG;
+  if (B <= 0 || max_len < 0 || total_rows <= 0 || h <= 0) return MLA_ERR_ARG;
+  if (!is_float_dtype(out_dtype)) return MLA_ERR_DTYPE;
+  if (h > 65535 || B > 65535 || total_rows > (int64_t)1 << 31) return MLA_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k_nope) || !aligned16(k_rope) || !aligned16(v) ||
+      !aligned16(out))
+    return MLA_ERR_ALIGN;
+  if (!mla::tc_device()) return MLA_ERR_DEVICE;
+  if (max_len == 0) return MLA_OK;
+  const float scale = softmax_scale > 0.f ? softmax_scale : (float)(1.0 / sqrt(192.0));
+  return from_cuda(mla::launch_prefill_tc(q, k_nope, k_rope, v, cu_seqlens, B, max_len, h,
+                                          total_rows, scale, out, out_dtype, lse, dev_status,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 int mla_cache_fill(const void* c_kv, const void* k_rope, int src_dtype,
                    const int32_t* cu_seqlens, int B, int max_len, const int32_t* block_table,
                    int max_blocks_per_seq, const mla_kv_cache* kv, double rope_theta,

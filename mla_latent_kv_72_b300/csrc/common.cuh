@@ -176,6 +176,14 @@ cudaError_t launch_linear_tc(const void* x, const void* w, void* y, int M, int K
 cudaError_t launch_fold_uv_o_tc(const void* w_uv, const void* w_o, void* w_fold, int h,
                                 int d_model, cudaStream_t s);
 
+// causal prefill attention in the MHA form (d_qk = 192, d_v = 128), bf16
+cudaError_t launch_prefill_tc(const void* q, const void* k_nope, const void* k_rope,
+                              const void* v, const int32_t* cu_seqlens, int B, int max_len,
+                              int h, int64_t total_rows, float scale, void* out, int out_dtype,
+                              float* lse, int32_t* status, cudaStream_t s);
+cudaError_t launch_prefill_query(const void* q_nope, const void* q_rope, const int32_t* cu_seqlens,
+                                 int B, int max_len, int h, double theta, void* q, cudaStream_t s);
+
 cudaError_t launch_decode_tc(const void* q_cat, const mla_kv_cache& kv,
                              const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                              int B, int q_len, int heads, int num_parts, float scale,

@@ -64,6 +64,7 @@ enum SetupKey : int {
   kSetupGemmMN = 2,       // ... of the per-head GEMM, MN-major A (absorb)
   kSetupGemmK = 3,        // ... of the per-head GEMM, K-major A (out_proj)
   kSetupAppend = 4,       // ... of the cache-append kernel
+  kSetupPrefill = 5,      // ... of the prefill attention kernel
   kSetupKeyCount
 };
 

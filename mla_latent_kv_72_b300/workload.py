@@ -278,3 +278,68 @@ class DeviceWorkload:
 
     def check_status(self) -> int:
         return int(self.status.item())
+
+
+class DevicePrefill:
+    """A prompt prefill of a workload's sequences in the MHA form, resident on
+    one GPU: the latent rows and rotated RoPE keys (written to the paged cache
+    and gathered back bit for bit), the per-head keys and values
+    k_nope = c W_UK^T and v = c W_UV^T (mla_linear), the queries
+    (mla_prefill_query) and the causal attention (mla_prefill_fwd)."""
+
+    def __init__(self, w: mi.Workload, device="cuda", out_dtype=torch.float32):
+        self.w = w
+        self.dw = DeviceWorkload(w, device=device)
+        dev = self.dw.device
+        lens = self.dw.lens_np
+        self.device = dev
+        self.lens_np = lens
+        self.T = int(lens.sum())
+        self.max_len = int(lens.max())
+        cu = np.zeros(w.B + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(lens)
+        self.cu = torch.from_numpy(cu).to(dev)
+        h = w.h
+        self.c = torch.empty((self.T, w.d_c), dtype=torch.bfloat16, device=dev)
+        self.k_rope = torch.empty((self.T, w.d_r), dtype=torch.bfloat16, device=dev)
+        C.mla_paged_gather(self.dw.kv, self.dw.block_table, self.cu, self.max_len, self.c,
+                           self.k_rope, dev_status=self.dw.status)
+        qn, qr = mi.prefill_queries(w, lens)
+        self.q_nope = storage_to_torch(qn, w.dtype, dev)
+        self.q_rope = storage_to_torch(qr, w.dtype, dev)
+        self.q = torch.empty((self.T, h, w.d_nope + w.d_r), dtype=torch.bfloat16, device=dev)
+        self.k_nope = torch.empty((self.T, h, w.d_nope), dtype=torch.bfloat16, device=dev)
+        self.v = torch.empty((self.T, h, w.d_v), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((self.T, h, w.d_v), dtype=out_dtype, device=dev)
+        self.lse = torch.empty((self.T, h), dtype=torch.float32, device=dev)
+        ws = max(C.mla_linear_workspace_bytes(self.T, w.d_c, h * w.d_nope),
+                 C.mla_linear_workspace_bytes(self.T, w.d_c, h * w.d_v))
+        self.ws = torch.empty(max(1, ws // 4), dtype=torch.float32, device=dev)
+        torch.cuda.synchronize(dev)
+
+    def keys_values(self, stream=None):
+        w = self.w
+        C.mla_linear(self.c, self.dw.w_uk.view(-1, w.d_c), self.k_nope.view(self.T, -1), self.ws,
+                     stream)
+        C.mla_linear(self.c, self.dw.w_uv.view(-1, w.d_c), self.v.view(self.T, -1), self.ws,
+                     stream)
+
+    def query(self, stream=None):
+        C.mla_prefill_query(self.q_nope, self.q_rope, self.cu, self.max_len, self.q,
+                            rope_theta=self.w.theta, stream=stream)
+
+    def attend(self, stream=None):
+        C.mla_prefill_fwd(self.q, self.k_nope, self.k_rope, self.v, self.cu, self.max_len,
+                          self.out, self.lse, dev_status=self.dw.status, stream=stream)
+
+    def run(self, stream=None):
+        self.keys_values(stream)
+        self.query(stream)
+        self.attend(stream)
+        return self.out
+
+    def attention_flops(self) -> float:
+        """Causal attention flops: 2 (192 + 128) per (query, visible key) pair per head."""
+        pairs = float(sum(int(L) * (int(L) + 1) // 2 for L in self.lens_np))
+        w = self.w
+        return 2.0 * (w.d_nope + w.d_r + w.d_v) * pairs * w.h

@@ -179,6 +179,45 @@ def decode_reference_multi(q_nope, q_rope, w_uk, w_uv, seqs, *, heads=None, scal
     return {"out": out, "o_lat": o_lat, "lse": lse}
 
 
+def prefill_reference(q_nope, q_rope, w_uk, w_uv, c, k_rope, *, heads=None, scale=None,
+                      theta=ROPE_THETA):
+    """Prefill of one sequence in the MHA form (kexue.fm "Part 3", eq. mla-mha,
+    used for training and prefill; iotdigitaltwinplm.com "Prefill versus
+    decode"): per head the keys k_i = [c_i W_kc^(s), RoPE(k_R,i, i)] (192-d)
+    and values v_i = c_i W_v^(s) (128-d) are formed, and every token t
+    attends causally to the tokens i <= t with its query
+    [q_nope,t, RoPE(q_R,t, t)] and the scale 1/sqrt(192).
+
+    q_nope [T, h, d_nope], q_rope [T, h, d_r] (unrotated, position t = row t),
+    c [T, d_c], k_rope [T, d_r] (unrotated pre-images).  Returns out
+    [T, H, d_v] and lse [T, H] (natural log of the causal softmax's
+    denominator).
+    """
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    q_rope = np.asarray(q_rope, dtype=np.float64)
+    c = np.asarray(c, dtype=np.float64)
+    w_uk = np.asarray(w_uk, dtype=np.float64)
+    w_uv = np.asarray(w_uv, dtype=np.float64)
+    T, h, d_nope = q_nope.shape
+    d_r = q_rope.shape[-1]
+    heads = list(range(h)) if heads is None else list(heads)
+    sc = score_scale(d_nope, d_r) if scale is None else scale
+    pos = np.arange(T)
+    k_r = rope(np.asarray(k_rope, dtype=np.float64), pos, theta)          # [T, d_r]
+    causal = pos[None, :] <= pos[:, None]                                 # [t, i]
+    out = np.zeros((T, len(heads), w_uv.shape[1]))
+    lse = np.zeros((T, len(heads)))
+    for j, s in enumerate(heads):
+        k = np.concatenate([c @ w_uk[s].T, k_r], axis=1)                 # [T, 192]
+        v = c @ w_uv[s].T                                                 # [T, d_v]
+        q = np.concatenate([q_nope[:, s], rope(q_rope[:, s], pos, theta)], axis=1)
+        z = np.where(causal, (q @ k.T) * sc, -np.inf)
+        p, l = softmax_with_lse(z)
+        out[:, j] = p @ v
+        lse[:, j] = l
+    return {"out": out, "lse": lse}
+
+
 def decode_absorbed(q_nope, q_rope, q_pos, w_uk, w_uv, seqs, *, heads=None,
                     scale=None, theta=ROPE_THETA):
     """Absorbed (MQA-form) MLA decode in float64.

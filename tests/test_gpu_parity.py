@@ -613,3 +613,39 @@ def test_step_from_hidden_state_matches_oracle(folded):
     y_ref, _ = O.decode_from_hidden(hid["x"], hid["w_dq"], hid["w_uq"], hid["w_qr"], inp["w_uk"],
                                     inp["w_uv"], hid["w_o"], inp["q_pos"], seqs)
     assert rel_err(y.cpu().numpy(), y_ref) <= TOL["bf16"]
+
+
+# ----------------------------------------------------------------------------
+# prefill in the MHA form (causal, d_qk = 192, d_v = 128)
+# ----------------------------------------------------------------------------
+
+PREFILL_CASES = {
+    # lengths around the 128-token tile: 1, 127, 128, 129, 300
+    "h4_edges": mi.scaled(mi.workload(3), B=5, h=4, L=None, lens=(1, 127, 128, 129, 300)),
+    "h16_ragged": mi.scaled(mi.workload(4), B=3, h=16, L_range=(200, 700)),
+}
+
+
+@pytest.mark.parametrize("name", list(PREFILL_CASES))
+def test_prefill_matches_oracle(name):
+    from mla_latent_kv_72_b300.workload import DevicePrefill
+    w = PREFILL_CASES[name]
+    pf = DevicePrefill(w)
+    pf.run()
+    torch.cuda.synchronize()
+    assert pf.dw.check_status() == 0
+    out = pf.out.cpu().numpy()
+    lse = pf.lse.cpu().numpy()
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    inp = O.workload_inputs_f64(w)
+    qn, qr = mi.prefill_queries(w)
+    qn = mi.storage_to_f64(qn, w.dtype)
+    qr = mi.storage_to_f64(qr, w.dtype)
+    cu = np.concatenate([[0], np.cumsum(pf.lens_np)])
+    for b in range(w.B):
+        L = int(pf.lens_np[b])
+        c, kr = O.sequence_view(w, b, L)
+        r = O.prefill_reference(qn[cu[b]:cu[b + 1]], qr[cu[b]:cu[b + 1]], inp["w_uk"],
+                                inp["w_uv"], c, kr)
+        assert rel_err(out[cu[b]:cu[b + 1]], r["out"]) <= TOL["bf16"], b
+        assert abs_err(lse[cu[b]:cu[b + 1]], r["lse"]) <= TOL["bf16"], b

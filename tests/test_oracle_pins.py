@@ -766,3 +766,28 @@ def test_decode_from_hidden_composes_the_steps():
                       [(c.tolist(), k.tolist()) for c, k in seqs])
     np.testing.assert_allclose(r["out"], bf, rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(y, bf.reshape(B, -1) @ wo.T, rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# prefill in the MHA form
+# ----------------------------------------------------------------------------
+
+def test_prefill_rows_equal_the_decode_of_their_prefix():
+    # row t of the causal prefill is the one-token decode of token t over the
+    # rows 0..t (the MHA form of the prefill and the decode form agree)
+    rng = np.random.default_rng(61)
+    T, h, d_c, d_r, d_nope, d_v = 9, 3, 8, 4, 5, 6
+    qn = rng.standard_normal((T, h, d_nope))
+    qr = rng.standard_normal((T, h, d_r))
+    wuk = rng.standard_normal((h, d_nope, d_c)) / 3
+    wuv = rng.standard_normal((h, d_v, d_c)) / 3
+    c = rng.standard_normal((T, d_c))
+    kr = rng.standard_normal((T, d_r))
+    ref = O.prefill_reference(qn, qr, wuk, wuv, c, kr)
+    for t in range(T):
+        d = O.decode_reference(qn[t][None], qr[t][None], [t], wuk, wuv, [(c[:t + 1], kr[:t + 1])])
+        np.testing.assert_allclose(ref["out"][t], d["out"][0], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(ref["lse"][t], d["lse"][0], rtol=1e-12)
+    # the first row sees only itself: its output is v_0 exactly
+    np.testing.assert_allclose(ref["out"][0], (c[0] @ wuv.transpose(0, 2, 1)).reshape(h, d_v),
+                               rtol=1e-12, atol=1e-14)
