@@ -463,6 +463,7 @@ def run_ours(args) -> None:
     e2e_value = aggregate(step_bytes * e2e_steps, world, e2e_s) / 1e9
 
     append = time_append(dw, stream, n_st)
+    hidden = time_hidden(dw, args.hidden) if args.hidden else None
 
     if rank != 0:
         return
@@ -507,6 +508,7 @@ def run_ours(args) -> None:
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "append": append,
+        "hidden": hidden,
         "gpu_launches": 4 * n_st,
         "clocks": clocks,
         "settle_s": args.settle_s,
@@ -574,6 +576,92 @@ def time_append(dw, stream, steps: int) -> dict:
             "timing": f"CUDA events around graph replays of {per_graph} launches"}
 
 
+def graph_time_us(fn, replays: int = 10, per_graph: int = 10) -> dict:
+    """Per-call GPU time of fn from CUDA-graph replays (no host launch overhead)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(replays)]
+    for a, b in ev:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 / per_graph for a, b in ev]
+    return {"mean_us": statistics.fmean(us), "median_us": statistics.median(us), "min_us": min(us)}
+
+
+def time_hidden(dw, spec: str) -> dict:
+    """The linear layers at the hidden-state boundary of the step (query
+    compression x -> c_q -> q_nope, q_rope; output W_UV then W_O, or the
+    merged W_O W_UV), per call, from CUDA-graph replays."""
+    d_model, d_cq = (int(v) for v in spec.split(","))
+    dw.enable_hidden(d_model, d_cq)
+    w = dw.w
+    res = {"d_model": d_model, "d_cq": d_cq}
+    res["query_from_hidden"] = graph_time_us(dw.query_from_hidden)
+    res["out_w_uv_then_w_o"] = graph_time_us(lambda: dw.hidden_out(False))
+    dw.hidden_out(True)   # forms the merged matrix once (outside the timing)
+    res["out_folded"] = graph_time_us(lambda: dw.hidden_out(True))
+    el = 2
+    res["weight_bytes"] = {
+        "w_dq_w_uq_w_qr": el * d_cq * (d_model + w.h * (w.d_nope + w.d_r)),
+        "w_uv_plus_w_o": el * w.h * w.d_v * (w.d_c + d_model),
+        "w_fold": el * w.h * w.d_c * d_model}
+    return res
+
+
+def run_prefill(args) -> None:
+    """--mode prefill: causal attention of whole prompts in the MHA form."""
+    import torch
+
+    import mla_inputs as mi
+    from mla_latent_kv_72_b300 import build as mbuild
+    from mla_latent_kv_72_b300.workload import DevicePrefill
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    mbuild.build()
+    w = resolve_workload(args.workload)
+    w = mi.scaled(w, B=args.batch if args.batch is not None else 4)
+    pf = DevicePrefill(w, device=f"cuda:{local}")
+    for _ in range(args.warmup):
+        pf.run()
+    torch.cuda.synchronize()
+    att = graph_time_us(pf.attend, replays=max(3, min(args.steps, 20)), per_graph=2)
+    kv = graph_time_us(pf.keys_values, replays=5, per_graph=2)
+    q = graph_time_us(pf.query, replays=5, per_graph=2)
+    assert pf.dw.check_status() == 0
+    peaks, peak_kind = load_peaks()
+    tc = float(peaks.get("bf16_tflops", PEAK_FALLBACK["bf16_tflops"]))
+    flops = pf.attention_flops()
+    t = att["mean_us"] * 1e-6
+    line = {"metric": "MLA prefill attention, MHA form (causal, d_qk=192, d_v=128): TFLOP/s",
+            "value": flops / t / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": att["mean_us"] / 1e3,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "h": w.h, "L": w.L,
+                       "tokens": pf.T, "mode": "prefill"},
+            "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": tc,
+                         "unit": "TFLOP/s", "frac": flops / t / 1e12 / tc,
+                         "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                         "kernel": "mla_prefill_fwd", "alg_flops": flops},
+            "attention": att, "keys_values_mla_linear": kv, "query": q}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None) -> None:
     p = argparse.ArgumentParser(description=__doc__)
     p.add_argument("--gpus", type=int, default=1)
@@ -591,6 +679,9 @@ def main(argv=None) -> None:
                    help="new tokens per sequence (multi-token decode; 1 = the one-token step)")
     p.add_argument("--settle-s", type=float, default=0.5,
                    help="seconds of untimed steps before the warm-up")
+    p.add_argument("--mode", choices=["decode", "prefill"], default="decode")
+    p.add_argument("--hidden", default=None,
+                   help="D_MODEL,D_CQ: also time the linear layers at the hidden-state boundary")
     p.add_argument("--cpu-budget", type=float, default=15.0,
                    help="seconds of oracle work for the CPU baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -599,6 +690,8 @@ def main(argv=None) -> None:
         p.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.mode == "prefill":
+        run_prefill(args)
     else:
         run_ours(args)
 
