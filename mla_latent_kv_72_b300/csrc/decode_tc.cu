@@ -41,7 +41,7 @@
 //                each) and meet on a 64-thread named barrier for the row max;
 //   warp 18      P.C MMA issuer: O_r += P C_r, 4 TS steps (P in TMEM, the
 //                latent boxes as an MN-major B operand), N = 256.
-// The FP8-latent variant has 3 bf16 stages, 2 e4m3 landing buffers, two
+// The FP8-latent variant has 3 bf16 stages, 2 e4m3 landing buffers, four
 // converter warps (e4m3 x block scale -> bf16 into the swizzled stage) and a
 // single event-driven MMA warp for both kinds of MMA.
 //

@@ -158,9 +158,12 @@ def _combine_f32(dw):
     return o.cpu().numpy(), lse.cpu().numpy()
 
 
-@pytest.mark.parametrize("num_parts", [1, 2, 7, 64, 148])
-def test_part_count_invariance(num_parts):
-    w = mi.scaled(mi.workload(3), B=2, h=128, L=3000)
+# (B, L, num_parts): the last case gives every sequence 74 chunks (296 parts
+# over 4 sequences of 128 blocks), the split-KV depth of the long-context use
+@pytest.mark.parametrize("B,L,num_parts", [(2, 3000, 1), (2, 3000, 2), (2, 3000, 7),
+                                           (2, 3000, 64), (2, 3000, 148), (4, 8192, 296)])
+def test_part_count_invariance(B, L, num_parts):
+    w = mi.scaled(mi.workload(3), B=B, h=128, L=L)
     dw1 = make(w, num_parts=1)
     dw1.step()
     dw = make(w, num_parts=num_parts)
