@@ -406,24 +406,32 @@ def run_ours(args) -> None:
         barrier()
         torch.cuda.synchronize()
         start.record(stream)
+        # events bracket the decode kernel every step; the step boundaries get
+        # events only when a flush runs between steps (otherwise start..end
+        # times the steps back to back, and fewer events mean fewer gaps)
         for i in range(n_st):
             if flush:
                 scrub.fill_(float(i))
-            ev[i][0].record(stream)
+                ev[i][0].record(stream)
             dw.absorb()
             ev[i][1].record(stream)
             dw.attend()
             ev[i][2].record(stream)
             dw.combine()
             dw.project()
-            ev[i][3].record(stream)
+            if flush:
+                ev[i][3].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
         barrier()
     clocks = clk.result()
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
     dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    total_s = (sum(step_ms) if flush else start.elapsed_time(end)) / 1e3
+    if flush:
+        step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+        total_s = sum(step_ms) / 1e3
+    else:
+        total_s = start.elapsed_time(end) / 1e3
+        step_ms = [total_s * 1e3 / n_st]       # back to back: the mean only
     max_total = reduce_max(total_s)
     assert dw.check_status() == 0
 
@@ -432,36 +440,69 @@ def run_ours(args) -> None:
     value = aggregate(step_bytes * n_st, world, max_total) / 1e9
     tflops = aggregate(step_flops * n_st, world, max_total) / 1e12
 
-    # end to end through the C ABI: pinned host inputs in, output back, every step
+    # end to end through the C ABI: every step copies its inputs in from pinned
+    # host memory and its output back.  Two sets of device inputs and outputs
+    # let the copies of steps k+1 and k-1 run on their own streams (the copy
+    # engines) while step k computes, as a decode loop would overlap them.
     h_qn = dw.q_nope.cpu().pin_memory()
     h_qr = dw.q_rope.cpu().pin_memory()
     h_pos = dw.q_pos.cpu().pin_memory()
-    h_out = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    h_out = [torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory() for _ in range(2)]
     h2d = h_qn.numel() * h_qn.element_size() + h_qr.numel() * h_qr.element_size() + \
         h_pos.numel() * h_pos.element_size()
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size()
     e2e_steps = max(3, min(n_st, 200))
+    d_in = [(dw.q_nope, dw.q_rope, dw.q_pos),
+            tuple(torch.empty_like(t) for t in (dw.q_nope, dw.q_rope, dw.q_pos))]
+    d_out = [dw.out, torch.empty_like(dw.out)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of set i landed
+    ev_used = [torch.cuda.Event() for _ in range(2)]    # the step using set i finished
+    ev_read = [torch.cuda.Event() for _ in range(2)]    # output of set i copied out
 
-    def e2e_step():
-        dw.q_nope.copy_(h_qn, non_blocking=True)
-        dw.q_rope.copy_(h_qr, non_blocking=True)
-        dw.q_pos.copy_(h_pos, non_blocking=True)
-        dw.step()
-        h_out.copy_(dw.out, non_blocking=True)
+    def e2e_step(k):
+        i = k % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_used[i])
+            for dst, src in zip(d_in[i], (h_qn, h_qr, h_pos)):
+                dst.copy_(src, non_blocking=True)
+            ev_in[i].record(s_in)
+        stream.wait_event(ev_in[i])
+        stream.wait_event(ev_read[i])
+        dw.q_nope, dw.q_rope, dw.q_pos = d_in[i]
+        dw.out = d_out[i]
+        dw.step(stream=stream)
+        ev_used[i].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_used[i])
+            h_out[i].copy_(d_out[i], non_blocking=True)
+            ev_read[i].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_join():
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    for k in range(3):
+        e2e_step(k)
+    e2e_join()
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for k in range(e2e_steps):
+        e2e_step(k)
+    e2e_join()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3)
     e2e_value = aggregate(step_bytes * e2e_steps, world, e2e_s) / 1e9
+    assert torch.equal(h_out[0], h_out[1])      # same inputs, same outputs
+    dw.q_nope, dw.q_rope, dw.q_pos = d_in[0]
+    dw.out = d_out[0]
 
+    breakdown = kernel_breakdown(dw, stream, flush, scrub)
     append = time_append(dw, stream, n_st)
     hidden = time_hidden(dw, args.hidden) if args.hidden else None
 
@@ -506,7 +547,10 @@ def run_ours(args) -> None:
         "step_ms": sstat,
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "copies": "pinned host buffers; inputs in and output out on two copy "
+                          "streams, double-buffered, overlapping the neighbouring steps"},
+        "kernels": breakdown,
         "append": append,
         "hidden": hidden,
         "gpu_launches": 4 * n_st,
@@ -600,6 +644,35 @@ def graph_time_us(fn, replays: int = 10, per_graph: int = 10) -> dict:
     torch.cuda.synchronize()
     us = [a.elapsed_time(b) * 1e3 / per_graph for a, b in ev]
     return {"mean_us": statistics.fmean(us), "median_us": statistics.median(us), "min_us": min(us)}
+
+
+def kernel_breakdown(dw, stream, flush: bool, scrub, steps: int = 50) -> dict:
+    """Per-kernel device time of the step (after the timed region): events
+    between the four launches of each of `steps` further steps, so that every
+    kernel sees the cache state it has inside a step (the weights of absorb
+    and out_proj come from HBM after the decode's stream has passed)."""
+    import torch
+    names = ("mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_out_proj")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for i in range(steps):
+        if flush:
+            scrub.fill_(float(i))
+        ev[i][0].record(stream)
+        dw.absorb()
+        ev[i][1].record(stream)
+        dw.attend()
+        ev[i][2].record(stream)
+        dw.combine()
+        ev[i][3].record(stream)
+        dw.project()
+        ev[i][4].record(stream)
+    torch.cuda.synchronize()
+    out = {}
+    for k, n in enumerate(names):
+        us = [e[k].elapsed_time(e[k + 1]) * 1e3 for e in ev]
+        out[n] = {"median_us": statistics.median(us), "min_us": min(us)}
+    out["steps"] = steps
+    return out
 
 
 def time_hidden(dw, spec: str) -> dict:

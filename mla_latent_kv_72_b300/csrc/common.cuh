@@ -78,6 +78,23 @@ __device__ __forceinline__ void rope_cos_sin(double pos, double inv_freq, float*
   sincosf(r, s, c);
 }
 
+// The same in float32 for an integer position 0 <= pos < 2^24, with the angle
+// measured in turns: pos * inv_freq / (2 pi) = pos * (f_hi + f_lo), f_hi and
+// f_lo the float32 head and tail of inv_freq / (2 pi) (formed in float64 on
+// the host).  Whole turns are removed exactly (Cody and Waite's additive
+// reduction, with the product kept exact inside the FMA): n is within one of
+// pos * f_hi, so |pos * f_hi - n| < 1 is rounded once (<= 2^-25 turns); the
+// tail adds pos * f_lo (< 1/8) with one more such rounding.  The angle error
+// is below 2 pi * 2^-23 turns ~ 7.5e-7 rad, then sincospif(2 t).
+__device__ __forceinline__ void rope_cos_sin_turns(int pos, float f_hi, float f_lo, float* c,
+                                                   float* s) {
+  const float p = (float)pos;
+  const float n = rintf(p * f_hi);
+  float t = fmaf(p, f_hi, -n);
+  t = fmaf(p, f_lo, t);
+  sincospif(2.0f * t, s, c);
+}
+
 // ---------------------------------------------------------------------------
 // work partition of the decode (shared by the decode kernels and the combine)
 // ---------------------------------------------------------------------------

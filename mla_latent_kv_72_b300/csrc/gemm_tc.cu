@@ -58,6 +58,8 @@ struct GemmParams {
   const uint16_t* q_rope;  // [B, h, 64] bf16 or null
   const int32_t* q_pos;
   double inv_freq[32];     // theta^(-2i/64), formed in float64 on the host
+  float turn_hi[32];       // inv_freq / (2 pi) as a float32 head + tail
+  float turn_lo[32];
   int32_t* status;
   long long wait_limit;
 };
@@ -151,21 +153,44 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
   __syncwarp();
 
   // rotary query part (absorb): independent of the MMA; the (row, pair) items
-  // of this head are spread over its m-tile CTAs, since the float64 angle
-  // reduction runs on the slow FP64 pipe
+  // of this head are spread over its m-tile CTAs.  A thread's items are
+  // loaded together, then rotated, so their load latencies overlap.
   if (p.q_rope != nullptr) {
     const int nb = min(p.n_tile, p.B - b0);
+    const int total = nb * 32;
+    const int stride = kGThreads * (int)gridDim.y;
     uint16_t* q_cat = static_cast<uint16_t*>(p.out);
-    for (int i = threadIdx.x + mt * kGThreads; i < nb * 32; i += kGThreads * (int)gridDim.y) {
-      const int bb = b0 + i / 32, pr = i % 32;
-      float cs, sn;
-      rope_cos_sin((double)p.q_pos[bb], p.inv_freq[pr], &cs, &sn);
-      const int64_t ib = ((int64_t)bb * p.h + s) * 64;
-      const float x0 = bf16_to_f32(p.q_rope[ib + 2 * pr]);
-      const float x1 = bf16_to_f32(p.q_rope[ib + 2 * pr + 1]);
-      const int64_t ob = ((int64_t)bb * p.h + s) * p.out_ld + 512 + 2 * pr;
-      q_cat[ob] = f32_to_bf16_rn(x0 * cs - x1 * sn);
-      q_cat[ob + 1] = f32_to_bf16_rn(x0 * sn + x1 * cs);
+    constexpr int kU = 4;
+    for (int i0 = threadIdx.x + mt * kGThreads; i0 < total; i0 += kU * stride) {
+      uint32_t xr[kU];
+      int32_t ps[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * stride;
+        if (i < total) {
+          const int bb = b0 + i / 32, pr = i % 32;
+          ps[u] = p.q_pos[bb];
+          xr[u] = *reinterpret_cast<const uint32_t*>(p.q_rope + ((int64_t)bb * p.h + s) * 64 +
+                                                    2 * pr);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * stride;
+        if (i >= total) break;
+        const int bb = b0 + i / 32, pr = i % 32;
+        float cs, sn;
+        if ((uint32_t)ps[u] < (1u << 24))
+          rope_cos_sin_turns(ps[u], p.turn_hi[pr], p.turn_lo[pr], &cs, &sn);
+        else
+          rope_cos_sin((double)ps[u], p.inv_freq[pr], &cs, &sn);
+        const float x0 = bf16_to_f32((uint16_t)(xr[u] & 0xffffu));
+        const float x1 = bf16_to_f32((uint16_t)(xr[u] >> 16));
+        const int64_t ob = ((int64_t)bb * p.h + s) * p.out_ld + 512 + 2 * pr;
+        *reinterpret_cast<uint32_t*>(q_cat + ob) =
+            (uint32_t)f32_to_bf16_rn(x0 * cs - x1 * sn) |
+            ((uint32_t)f32_to_bf16_rn(x0 * sn + x1 * cs) << 16);
+      }
     }
   }
 
@@ -326,7 +351,12 @@ cudaError_t launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int
   p.out_dtype = MLA_BF16;
   p.q_rope = static_cast<const uint16_t*>(q_rope);
   p.q_pos = q_pos;
-  for (int i = 0; i < 32; ++i) p.inv_freq[i] = pow(theta, -2.0 * (double)i / 64.0);
+  for (int i = 0; i < 32; ++i) {
+    p.inv_freq[i] = pow(theta, -2.0 * (double)i / 64.0);
+    const double turns = p.inv_freq[i] / 6.283185307179586476925;
+    p.turn_hi[i] = (float)turns;
+    p.turn_lo[i] = (float)(turns - (double)p.turn_hi[i]);
+  }
   p.status = nullptr;
   p.wait_limit = 4000000000LL;
   dim3 grid(h, 512 / 128, ceil_div(B, nt));
