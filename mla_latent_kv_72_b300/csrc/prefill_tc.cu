@@ -11,20 +11,28 @@
 // k_nope = C W_UK^T and v = C W_UV^T come from mla_linear; this kernel is the
 // attention.
 //
-// One CTA per (128-query tile, head, sequence); 320 threads:
-//   warp 0      TMA: the Q tile once (3 boxes of 64 dims x 128 tokens), then
-//               the K (k_nope 2 boxes + the shared RoPE key 1 box) and V (2
-//               boxes) tiles of 128 tokens into a ring of 2 stages;
-//   warp 1      MMA issuer: S(j) = Q K(j)^T (12 K=16 steps, M = 128 queries,
-//               N = 128 keys) into S buffer j % 2, and O += P(j) V(j) (8 steps,
-//               P from TMEM, V as an MN-major operand);
-//   warps 2..9  softmax: two warps per TMEM lane quarter split a row's 128
-//               scores (64 each); online softmax with a lazily rescaled O
-//               (only when the maximum grows by more than kTau, log2 units).
-// TMEM columns: S x 2 [0, 256), O [256, 384), P (bf16 pairs) [384, 448).
-// Key tiles past the query tile are skipped; the diagonal tile is masked to
-// keys i <= t.  Every wait is bounded; a timeout is written to the status
-// word and the kernel winds down.
+// One CTA per (256 queries, head, sequence): two query tiles of 128 rows, A
+// (the first 128) and B (the next), 576 threads:
+//   warp 0      TMA: both query tiles once (3 boxes of 64 dims x 128 tokens
+//               each), then per key tile of 128 tokens the K boxes (k_nope 2 +
+//               the shared RoPE key 1) and the V boxes (2) into a ring of 8
+//               slots of 16 KB (a V tile takes two neighbouring slots);
+//   warp 1      MMA issuer: S_t(j) = Q_t K(j)^T (12 K=16 steps, M = 128
+//               queries, N = 128 keys) and O_t += P_t(j) V(j) (8 steps, P from
+//               TMEM, V as an MN-major operand), in the order PV_A(j),
+//               S_A(j+1), PV_B(j), S_B(j+1): while one tile's softmax runs, the
+//               tensor cores work on the other tile;
+//   warps 2..17 softmax, 8 warps per query tile: two warps per TMEM lane
+//               quarter split a row's 128 scores (64 each); online softmax
+//               with a lazily rescaled O (only when the maximum grows by more
+//               than kTau, log2 units).
+// TMEM columns: tile t holds S_t at [256 t, 256 t + 128) and O_t at
+// [256 t + 128, 256 t + 256); P_t (bf16 pairs, 64 columns) is written over
+// the first half of S_t once the scores are in registers.  The MMAs of one
+// issuing thread run in issue order, so S_t(j+1) overwrites P_t(j) only after
+// O_t += P_t(j) V(j) has read it.  Key tiles past a query tile are skipped; the
+// diagonal tile is masked to keys i <= t.  Every wait is bounded; a timeout
+// is written to the status word and the kernel winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -41,46 +49,64 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTile = 128;                  // queries per CTA and keys per tile
+constexpr int kTile = 128;                  // queries per tile and keys per key tile
+constexpr int kQTiles = 2;                  // query tiles per CTA
 constexpr int kBox = 128 * 128;             // 128 rows x 64 bf16, 128-byte swizzle (16 KB)
-constexpr int kQBytes = 3 * kBox;           // 192 dims
-constexpr int kKBytes = 3 * kBox;           // 128 nope dims + 64 RoPE dims
-constexpr int kVBytes = 2 * kBox;           // 128 dims
-constexpr int kStageBytes = kKBytes + kVBytes;
-constexpr int kStages = 2;
-constexpr int kThreads = 320;
-constexpr int kSoftWarps = 8;
-constexpr int kOffQ = 0;
-constexpr int kOffStages = kOffQ + kQBytes;
-constexpr int kOffHmax = kOffStages + kStages * kStageBytes;    // [2][128] float
-constexpr int kOffLsum = kOffHmax + 2 * 128 * 4;                // [128] float
-constexpr int kOffBar = kOffLsum + 128 * 4;
-constexpr int kNumBars = 16;
+constexpr int kQBytes = 3 * kBox;           // one query tile, 192 dims
+constexpr int kSlots = 8;                   // K/V ring slots of one box each
+constexpr int kSoftWarps = 8;               // per query tile
+constexpr int kThreads = 64 + 32 * kSoftWarps * kQTiles;
+constexpr int kOffQ = 0;                    // [kQTiles] query tiles
+constexpr int kOffRing = kOffQ + kQTiles * kQBytes;
+constexpr int kOffHm = kOffRing + kSlots * kBox;   // [kQTiles][128] float: row max / row sum meeting
+constexpr int kOffBar = kOffHm + kQTiles * 128 * 4;
+constexpr int kNumBars = 32;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
-constexpr uint32_t kColS = 0;     // [2] 128 columns each
-constexpr uint32_t kColO = 256;
-constexpr uint32_t kColP = 384;   // 64 columns: 128 keys as bf16 pairs
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 512;        // tile t: S_t / P_t at 256 t, O_t at 256 t + 128
 
 constexpr float kTau = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 enum {
   BAR_Q_FULL = 0,
-  BAR_KV_FULL = 1,                // [2]
-  BAR_KV_EMPTY = BAR_KV_FULL + 2, // [2]
-  BAR_S_FULL = BAR_KV_EMPTY + 2,  // [2]
-  BAR_S_EMPTY = BAR_S_FULL + 2,   // [2] softmax warps read S buffer j % 2
-  BAR_P_FULL = BAR_S_EMPTY + 2,   // softmax warps stored P(j)
-  BAR_O_DONE = BAR_P_FULL + 1,    // [2] O += P(j) V(j) done (by j % 2)
-  BAR_DRAIN = BAR_O_DONE + 2,
+  BAR_FULL = 1,                         // [kSlots] TMA -> MMA
+  BAR_EMPTY = BAR_FULL + kSlots,        // [kSlots] MMA -> TMA
+  BAR_S_FULL = BAR_EMPTY + kSlots,      // [kQTiles] S_t(j) written
+  BAR_P_FULL = BAR_S_FULL + kQTiles,    // [kQTiles] softmax warps of tile t stored P_t(j)
+  BAR_O_DONE = BAR_P_FULL + kQTiles,    // [kQTiles] last O_t += P_t V done
+  BAR_DRAIN = BAR_O_DONE + kQTiles,
   BAR_COUNT = BAR_DRAIN + 1,
 };
 static_assert(BAR_COUNT <= kNumBars, "barrier array");
+
+// Slot sequence of the K/V ring, walked identically by the TMA producer and
+// the MMA issuer: per key tile three single slots (K) and one pair of
+// neighbouring slots (V; a pair never starts on the last slot, which is then
+// skipped).  phase bit s = parity of slot s's fills so far, used bit s = slot
+// s filled before (its refill waits for the previous use to end).
+struct Ring {
+  int pos = 0;
+  uint32_t phase = 0, used = 0;
+  __device__ __forceinline__ int next(bool pair) {
+    int s = pos % kSlots;
+    if (pair && s == kSlots - 1) {
+      ++pos;
+      s = 0;
+    }
+    pos += pair ? 2 : 1;
+    return s;
+  }
+  __device__ __forceinline__ uint32_t parity(int s) const { return (phase >> s) & 1u; }
+  __device__ __forceinline__ bool was_used(int s) const { return (used >> s) & 1u; }
+  __device__ __forceinline__ void advance(int s) {
+    phase ^= 1u << s;
+    used |= 1u << s;
+  }
+};
 
 struct PrefillParams {
   const int32_t* cu_seqlens;
@@ -113,14 +139,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int qt = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+  // the longest CTAs (last query tiles: most key tiles) are launched first
+  const int m = (int)gridDim.x - 1 - (int)blockIdx.x;
+  const int s = blockIdx.y, b = blockIdx.z;
   const int row_begin = p.cu_seqlens[b];
   const int L = p.cu_seqlens[b + 1] - row_begin;
-  const int q0 = qt * kTile;               // first query position of this CTA
+  const int q0 = m * kQTiles * kTile;      // first query position of this CTA
   if (q0 >= L) return;                     // uniform for the whole CTA
-  const int n_q = min(kTile, L - q0);      // live query rows
-  const int ntiles = qt + 1;               // key tiles 0 .. qt (causal)
-  const int r0 = row_begin + q0;           // global row of query 0 / of key tile qt
+  // key tiles of query tile t: 0 .. 2m + t (causal); tile B may be past the end
+  const int ntk0 = kQTiles * m + 1;
+  const int ntk1 = q0 + kTile < L ? kQTiles * m + 2 : 0;
+  auto ntk = [&](int t) { return t == 0 ? ntk0 : ntk1; };
+  const int nkt = ntk1 > ntk0 ? ntk1 : ntk0;
 
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8 * i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -128,14 +158,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q_FULL), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(BAR_KV_FULL + i), 1);
-      mbar_init(bar(BAR_KV_EMPTY + i), 1);
-      mbar_init(bar(BAR_S_FULL + i), 1);
-      mbar_init(bar(BAR_S_EMPTY + i), kSoftWarps);
-      mbar_init(bar(BAR_O_DONE + i), 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(bar(BAR_FULL + i), 1);
+      mbar_init(bar(BAR_EMPTY + i), 1);
     }
-    mbar_init(bar(BAR_P_FULL), kSoftWarps);
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(bar(BAR_S_FULL + t), 1);
+      mbar_init(bar(BAR_P_FULL + t), kSoftWarps);
+      mbar_init(bar(BAR_O_DONE + t), 1);
+    }
     mbar_init(bar(BAR_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -159,83 +190,140 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (lane == 0) ok = mbar_wait_or_abort(bb, parity, lim, abort_flag, &timed_out);
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   };
+  const uint32_t ring = sbase + kOffRing;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(BAR_Q_FULL), kQBytes);
-      for (int c = 0; c < 3; ++c)
-        tma_load_3d(sbase + kOffQ + c * kBox, &tm_q, 64 * c, s, r0, bar(BAR_Q_FULL));
-      int j = 0;
-      for (; j < ntiles; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages && !mbar_wait_or_abort(bar(BAR_KV_EMPTY + st), ((j / kStages) - 1) & 1,
-                                                lim, abort_flag, &timed_out)) {
-          fail();
-          break;
-        }
-        const uint32_t dst = sbase + kOffStages + st * kStageBytes;
+      const int r0 = row_begin + q0;
+      mbar_arrive_expect_tx(bar(BAR_Q_FULL), kQTiles * kQBytes);
+      for (int t = 0; t < kQTiles; ++t)
+        for (int c = 0; c < 3; ++c)
+          tma_load_3d(sbase + kOffQ + t * kQBytes + c * kBox, &tm_q, 64 * c, s, r0 + t * kTile,
+                      bar(BAR_Q_FULL));
+      Ring rg;
+      bool ok = true;
+      auto fill = [&](int slot) -> bool {
+        if (rg.was_used(slot) && !mbar_wait_or_abort(bar(BAR_EMPTY + slot), rg.parity(slot) ^ 1u,
+                                                     lim, abort_flag, &timed_out))
+          return false;
+        mbar_arrive_expect_tx(bar(BAR_FULL + slot), kBox);
+        return true;
+      };
+      for (int j = 0; ok && j < nkt; ++j) {
         const int kr = row_begin + j * kTile;   // global row of key 0 of tile j
-        mbar_arrive_expect_tx(bar(BAR_KV_FULL + st), kStageBytes);
-        tma_load_3d(dst, &tm_kn, 0, s, kr, bar(BAR_KV_FULL + st));
-        tma_load_3d(dst + kBox, &tm_kn, 64, s, kr, bar(BAR_KV_FULL + st));
-        tma_load_2d(dst + 2 * kBox, &tm_kr, 0, kr, bar(BAR_KV_FULL + st));
-        tma_load_3d(dst + kKBytes, &tm_v, 0, s, kr, bar(BAR_KV_FULL + st));
-        tma_load_3d(dst + kKBytes + kBox, &tm_v, 64, s, kr, bar(BAR_KV_FULL + st));
+        for (int c = 0; c < 3 && ok; ++c) {
+          const int sl = rg.next(false);
+          if (!(ok = fill(sl))) break;
+          if (c < 2)
+            tma_load_3d(ring + sl * kBox, &tm_kn, 64 * c, s, kr, bar(BAR_FULL + sl));
+          else
+            tma_load_2d(ring + sl * kBox, &tm_kr, 0, kr, bar(BAR_FULL + sl));
+          rg.advance(sl);
+        }
+        if (!ok) break;
+        const int sv = rg.next(true);
+        for (int c = 0; c < 2 && ok; ++c) {
+          if (!(ok = fill(sv + c))) break;
+          tma_load_3d(ring + (sv + c) * kBox, &tm_v, 64 * c, s, kr, bar(BAR_FULL + sv + c));
+          rg.advance(sv + c);
+        }
       }
+      if (!ok) fail();
       // every issued copy lands before the CTA may leave
       int never = 0;
       bool dummy = false;
       mbar_wait_or_abort(bar(BAR_Q_FULL), 0, lim, &never, &dummy);
-      for (int st = 0; st < kStages; ++st) {
-        const int n = (j - st + kStages - 1) / kStages;
-        if (n > 0) mbar_wait_or_abort(bar(BAR_KV_FULL + st), (n - 1) & 1, lim, &never, &dummy);
-      }
+      for (int sl = 0; sl < kSlots; ++sl)
+        if (rg.was_used(sl))
+          mbar_wait_or_abort(bar(BAR_FULL + sl), rg.parity(sl) ^ 1u, lim, &never, &dummy);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // in order: S(j), then O += P(j-1) V(j-1); S(j) needs its stage and the
-    // softmax's read of S(j-2); P(j-1) is written after O += P(j-2) V(j-2)
     const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
     const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
+    Ring rg;
+    int ks0 = 0, ks1 = 0, ks2 = 0, sv = 0;
+    auto ks = [&](int c) { return c == 0 ? ks0 : (c == 1 ? ks1 : ks2); };
     bool ok = warp_wait(bar(BAR_Q_FULL), 0);
-    auto issue_pv = [&](int jj) -> bool {
-      if (!warp_wait(bar(BAR_P_FULL), jj & 1)) return false;
+    auto acquire_k = [&]() -> bool {
+      ks0 = rg.next(false);
+      ks1 = rg.next(false);
+      ks2 = rg.next(false);
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        if (!warp_wait(bar(BAR_FULL + ks(c)), rg.parity(ks(c)))) return false;
+        rg.advance(ks(c));
+      }
+      return true;
+    };
+    auto acquire_v = [&]() -> bool {
+      sv = rg.next(true);
+      for (int c = 0; c < 2; ++c) {
+        if (!warp_wait(bar(BAR_FULL + sv + c), rg.parity(sv + c))) return false;
+        rg.advance(sv + c);
+      }
+      return true;
+    };
+    auto release = [&](int sl) {
+      if (lane == 0) mma_commit(bar(BAR_EMPTY + sl));
+    };
+    auto issue_s = [&](int t) {
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t v_st = sbase + kOffStages + (jj % kStages) * kStageBytes + kKBytes;
+        const uint32_t q_t = sbase + kOffQ + t * kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < 12; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          const uint64_t ad = smem_desc(q_t + (kk >> 2) * kBox + off, 16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(ring + ks(kk >> 2) * kBox + off, 16, 1024, kSwizzle128B);
+          mma_ss(tmem + 256 * t, ad, bd, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(BAR_S_FULL + t));
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int t, int j) -> bool {
+      if (!warp_wait(bar(BAR_P_FULL + t), j & 1)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t v_st = ring + sv * kBox;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t bd = smem_desc(v_st + kk * 2048, kBox, 1024, kSwizzle128B);
-          mma_ts(tmem + kColO, tmem + kColP + 8 * kk, bd, idO, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + 256 * t + 128, tmem + 256 * t + 8 * kk, bd, idO,
+                 (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(BAR_O_DONE + (jj & 1)));
-        mma_commit(bar(BAR_KV_EMPTY + (jj % kStages)));
+        if (j == ntk(t) - 1) mma_commit(bar(BAR_O_DONE + t));
       }
       __syncwarp();
       return true;
     };
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const int st = j % kStages;
-      if (!warp_wait(bar(BAR_KV_FULL + st), (j / kStages) & 1)) { ok = false; break; }
-      if (j >= 2 && !warp_wait(bar(BAR_S_EMPTY + (j & 1)), ((j >> 1) - 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t k_st = sbase + kOffStages + st * kStageBytes;
-        const uint32_t d = tmem + kColS + 128 * (j & 1);
-#pragma unroll
-        for (int kk = 0; kk < 12; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          const uint64_t ad = smem_desc(sbase + kOffQ + off, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(k_st + off, 16, 1024, kSwizzle128B);
-          mma_ss(d, ad, bd, idS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(BAR_S_FULL + (j & 1)));
-      }
-      __syncwarp();
-      if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+    if (ok) ok = acquire_k();
+    if (ok) {
+      for (int t = 0; t < kQTiles; ++t)
+        if (ntk(t) > 0) issue_s(t);
+      for (int c = 0; c < 3; ++c) release(ks(c));
     }
-    if (ok && !issue_pv(ntiles - 1)) ok = false;
+    for (int j = 0; ok && j < nkt; ++j) {
+      if (!(ok = acquire_v())) break;
+      const bool more = j + 1 < nkt;
+      bool have_k = false;
+      for (int t = 0; t < kQTiles && ok; ++t) {
+        if (j < ntk(t) && !(ok = issue_pv(t, j))) break;
+        if (j + 1 < ntk(t)) {
+          if (!have_k) {
+            if (!(ok = acquire_k())) break;
+            have_k = true;
+          }
+          issue_s(t);
+        }
+      }
+      if (!ok) break;
+      for (int c = 0; c < 2; ++c) release(sv + c);
+      if (more && have_k)
+        for (int c = 0; c < 3; ++c) release(ks(c));
+    }
     if (!ok) fail();
     if (lane == 0) {
       mma_commit(bar(BAR_DRAIN));
@@ -246,30 +334,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int wg = warp - 2;              // 0..7
-    const int hf = wg >> 2;               // column half: keys [64 hf, 64 hf + 64)
+    const int w = warp - 2;               // 0..15
+    const int t = w / kSoftWarps;         // query tile
+    const int hf = (w % kSoftWarps) >> 2; // column half: keys [64 hf, 64 hf + 64)
     const int sub = warp & 3;             // TMEM lane quarter
     const int row = sub * 32 + lane;      // query row of the tile
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
-    float* hmax = reinterpret_cast<float*>(smem + kOffHmax);
-    float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
-    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + sub) : "memory"); };
+    const uint32_t colS = 256 * t, colO = 256 * t + 128;
+    float* hm = reinterpret_cast<float*>(smem + kOffHm) + t * 128;
+    const int barid = 1 + t * 4 + sub;
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(barid) : "memory"); };
+    // the two halves of a row meet in hm[row]: half 1 writes, half 0 combines
+    // and writes back, half 1 reads (two meetings)
+    auto meet = [&](float v, bool is_max) -> float {
+      if (hf == 1) hm[row] = v;
+      pair_sync();
+      if (hf == 0) {
+        v = is_max ? fmaxf(v, hm[row]) : v + hm[row];
+        hm[row] = v;
+      }
+      pair_sync();
+      if (hf == 1) v = hm[row];
+      return v;
+    };
+    const int n = ntk(t);
+    const int qt_diag = kQTiles * m + t;  // key tile on the diagonal
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntiles && ok; ++j) {
-      if (!warp_wait(bar(BAR_S_FULL + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+    for (int j = 0; j < n && ok; ++j) {
+      if (!warp_wait(bar(BAR_S_FULL + t), j & 1)) { ok = false; break; }
       tc_fence_after();
       uint32_t r[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        tmem_ld16(tl + kColS + 128 * (j & 1) + 64 * hf + 16 * c,
-                  *reinterpret_cast<uint32_t(*)[16]>(&r[16 * c]));
+        tmem_ld16(tl + colS + 64 * hf + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * c]));
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_S_EMPTY + (j & 1)));
       // scores in log2 units; the diagonal tile sees keys i <= t only
-      const bool diag = j == qt;
+      const bool diag = j == qt_diag;
       float mt = -INFINITY;
 #pragma unroll
       for (int kk = 0; kk < 64; ++kk) {
@@ -278,11 +379,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         r[kk] = __float_as_uint(x);
         mt = fmaxf(mt, x);
       }
-      // row maximum over both halves
-      pair_sync();
-      hmax[hf * 128 + row] = mt;
-      pair_sync();
-      mt = fmaxf(mt, hmax[(hf ^ 1) * 128 + row]);
+      mt = meet(mt, true);
       float m_new = m_run;
       bool resc = false;
       if (m_run == -INFINITY) {
@@ -300,57 +397,44 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         psum += p0 + p1;
         r[e] = pack_bf16x2(p0, p1);
       }
-      // P's TMEM columns and O are free once O += P(j-1) V(j-1) is done
-      if (j >= 1) {
-        const int jp = j - 1;
-        if (!warp_wait(bar(BAR_O_DONE + (jp & 1)), (jp >> 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-      }
-      if (resc) {
-        const float alpha = exp2f(m_run - m_new);
-        l_run *= alpha;
-      }
+      // O_t is final for P_t(j-1) here: S_t(j) was issued after O_t += P_t(j-1) V
+      if (resc) l_run *= exp2f(m_run - m_new);
       if (__any_sync(0xffffffffu, resc)) {
         const float alpha = resc ? exp2f(m_run - m_new) : 1.0f;
         for (int c = 0; c < 4; ++c) {
           uint32_t v[16];
-          tmem_ld16(tl + kColO + 64 * hf + 16 * c, v);
+          tmem_ld16(tl + colO + 64 * hf + 16 * c, v);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st16(tl + kColO + 64 * hf + 16 * c, v);
+          tmem_st16(tl + colO + 64 * hf + 16 * c, v);
         }
       }
       m_run = m_new;
       l_run += psum;
+      // P over the first half of S: both halves of every row have read their
+      // scores (they met above)
 #pragma unroll
       for (int c = 0; c < 2; ++c)
-        tmem_st16(tl + kColP + 32 * hf + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * c]));
+        tmem_st16(tl + colS + 32 * hf + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * c]));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P_FULL));
+      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + t));
     }
-    if (ok) {
+    if (ok && n > 0) {
       // ---- epilogue: O / l -> out rows, lse
-      const int jl = ntiles - 1;
-      ok = warp_wait(bar(BAR_O_DONE + (jl & 1)), (jl >> 1) & 1);
+      ok = warp_wait(bar(BAR_O_DONE + t), 0);
       if (ok) {
         tc_fence_after();
-        pair_sync();
-        if (hf == 1) lsum[row] = l_run;
-        pair_sync();
-        const float l = hf == 0 ? l_run + lsum[row] : 0.f;
-        pair_sync();
-        if (hf == 0) lsum[row] = l;
-        pair_sync();
-        const float lt = lsum[row];
+        const float lt = meet(l_run, false);
         const float inv = lt > 0.f ? 1.0f / lt : 0.f;
-        const bool live = row < n_q;
-        const int64_t orow = ((int64_t)(r0 + row) * p.h + s) * 128 + 64 * hf;
+        const int qpos = q0 + t * kTile + row;
+        const bool live = qpos < L;
+        const int64_t orow = ((int64_t)(row_begin + qpos) * p.h + s) * 128 + 64 * hf;
         for (int c = 0; c < 4; ++c) {
           uint32_t v[16];
-          tmem_ld16(tl + kColO + 64 * hf + 16 * c, v);
+          tmem_ld16(tl + colO + 64 * hf + 16 * c, v);
           tmem_wait_ld();
           if (live) {
             if (p.out_dtype == MLA_F32) {
@@ -362,24 +446,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                 __uint_as_float(v[4 * q4 + 2]) * inv, __uint_as_float(v[4 * q4 + 3]) * inv);
             } else {
               uint16_t* o = static_cast<uint16_t*>(p.out) + orow + 16 * c;
-              uint32_t w[8];
+              uint32_t w8[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e)
-                w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
-              *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
-              *reinterpret_cast<uint4*>(o + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                w8[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv, __uint_as_float(v[2 * e + 1]) * inv);
+              *reinterpret_cast<uint4*>(o) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+              *reinterpret_cast<uint4*>(o + 8) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
             }
           }
         }
         if (live && hf == 0 && p.lse != nullptr)
-          p.lse[(int64_t)(r0 + row) * p.h + s] = lt > 0.f ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
+          p.lse[(int64_t)(row_begin + qpos) * p.h + s] =
+              lt > 0.f ? (m_run + log2f(lt)) * kLn2 : -INFINITY;
       }
     }
     if (!ok) {
       fail();
       // the partner warp of this lane quarter may wait at a pair meeting
-      asm volatile("bar.arrive %0, 64;" ::"r"(1 + sub) : "memory");
-      asm volatile("bar.arrive %0, 64;" ::"r"(1 + sub) : "memory");
+      asm volatile("bar.arrive %0, 64;" ::"r"(barid) : "memory");
+      asm volatile("bar.arrive %0, 64;" ::"r"(barid) : "memory");
     }
   }
 
@@ -460,7 +545,7 @@ cudaError_t launch_prefill_tc(const void* q, const void* k_nope, const void* k_r
   if (r != 0) return r < 0 ? cudaErrorInvalidDevice : (cudaError_t)r;
   PrefillParams p{cu_seqlens, out, out_dtype, lse, h, scale * 1.4426950408889634f, status,
                   4000000000LL};
-  dim3 grid(ceil_div(max_len, kTile), h, B);
+  dim3 grid(ceil_div(max_len, kQTiles * kTile), h, B);
   prefill_tc_kernel<<<grid, kThreads, kSmemAlloc, s>>>(tq, tkn, tkr, tv, p);
   return cudaGetLastError();
 }

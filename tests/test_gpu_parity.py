@@ -626,6 +626,9 @@ PREFILL_CASES = {
     # lengths around the 128-token tile: 1, 127, 128, 129, 300
     "h4_edges": mi.scaled(mi.workload(3), B=5, h=4, L=None, lens=(1, 127, 128, 129, 300)),
     "h16_ragged": mi.scaled(mi.workload(4), B=3, h=16, L_range=(200, 700)),
+    # up to 17 key tiles per query tile: the K/V ring wraps many times, and
+    # the last CTA of each sequence has only its first query tile
+    "h2_long": mi.scaled(mi.workload(3), B=2, h=2, L=None, lens=(1500, 2100)),
 }
 
 
