@@ -232,14 +232,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_kn, const __grid_consta
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-    const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
-    bool ok = warp_spin(bar(BAR_Q_READY), 0);
-    auto issue_s = [&](int j) -> bool {
-      const int st = j % kKStages;
-      if (!warp_spin(bar(BAR_K_FULL + st), (j / kKStages) & 1)) return false;
-      tc_fence_after();
-      if (lane == 0) {
+    // one thread runs the whole loop: a warp-wide loop (the other lanes waiting
+    // at warp reconvergence and a broadcast after every wait) was measured to
+    // add several hundred cycles per key tile to the MMA issue
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
+      auto wait = [&](uint32_t bb, uint32_t parity) -> bool {
+        return mbar_spin_or_abort(bb, parity, lim, abort_flag, &timed_out);
+      };
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kKStages;
+        if (!wait(bar(BAR_K_FULL + st), (j / kKStages) & 1)) return false;
+        tc_fence_after();
         const uint32_t k_st = sbase + kOffK + st * kKBytes;
         const uint32_t d = tmem + kColS + 128 * (j & 1);
 #pragma unroll
@@ -250,16 +255,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_kn, const __grid_consta
         }
         mma_commit(bar(BAR_S_FULL + (j & 1)));
         mma_commit(bar(BAR_K_EMPTY + st));
-      }
-      __syncwarp();
-      return true;
-    };
-    auto issue_pv = [&](int j) -> bool {
-      const int st = j % kVStages;
-      if (!warp_spin(bar(BAR_V_FULL + st), (j / kVStages) & 1)) return false;
-      if (!warp_spin(bar(BAR_P_FULL + (j & 1)), (j >> 1) & 1)) return false;
-      tc_fence_after();
-      if (lane == 0) {
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int st = j % kVStages;
+        if (!wait(bar(BAR_V_FULL + st), (j / kVStages) & 1)) return false;
+        if (!wait(bar(BAR_P_FULL + (j & 1)), (j >> 1) & 1)) return false;
+        tc_fence_after();
         const uint32_t v_st = sbase + kOffV + st * kVBytes;
         const uint32_t a = tmem + kColS + 128 * (j & 1);
 #pragma unroll
@@ -269,17 +271,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_kn, const __grid_consta
         }
         mma_commit(bar(BAR_O_DONE));
         mma_commit(bar(BAR_V_EMPTY + st));
+        return true;
+      };
+      bool ok = wait(bar(BAR_Q_READY), 0);
+      for (int j = 0; ok && j < 2 && j < n; ++j) ok = issue_s(j);
+      for (int j = 0; ok && j < n; ++j) {
+        if (!(ok = issue_pv(j))) break;
+        if (j + 2 < n) ok = issue_s(j + 2);
       }
-      __syncwarp();
-      return true;
-    };
-    for (int j = 0; ok && j < 2 && j < n; ++j) ok = issue_s(j);
-    for (int j = 0; ok && j < n; ++j) {
-      if (!(ok = issue_pv(j))) break;
-      if (j + 2 < n) ok = issue_s(j + 2);
-    }
-    if (!ok) fail();
-    if (lane == 0) {
+      if (!ok) fail();
       mma_commit(bar(BAR_DRAIN));
       int never = 0;
       bool dummy = false;
