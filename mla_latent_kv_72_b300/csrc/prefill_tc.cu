@@ -341,17 +341,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_kn, const __grid_consta
       tmem_ld16(tl + kColS + 128 * sb + 32 * cq + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16]));
       tmem_wait_ld();
       // raw-score maximum (the scale is positive); the diagonal tile sees keys i <= t only
-      float mt = -INFINITY;
       if (j == qt) {
 #pragma unroll
-        for (int kk = 0; kk < kCols; ++kk) {
+        for (int kk = 0; kk < kCols; ++kk)
           if (32 * cq + kk > row) r[kk] = __float_as_uint(-INFINITY);
-          mt = fmaxf(mt, __uint_as_float(r[kk]));
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < kCols; ++kk) mt = fmaxf(mt, __uint_as_float(r[kk]));
       }
+      // four independent chains, then a tree (the maximum is exact in any order)
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int kk = 0; kk < kCols; ++kk) m4[kk & 3] = fmaxf(m4[kk & 3], __uint_as_float(r[kk]));
+      float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       // the four quarters of the row meet (buffer j % 2, so one meeting per tile)
       float* hmb = hm + sb * kQuarterWarps * 128;
       hmb[cq * 128 + row] = mt;
@@ -368,14 +367,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_kn, const __grid_consta
       }
       const float mb = m_new * sl2;
       // P = 2^(x * scale_log2 - m * scale_log2) as bf16 pairs, row sum share
-      float psum = 0.f;
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int e = 0; e < kCols / 2; ++e) {
         const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), sl2, -mb));
         const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, -mb));
-        psum += p0 + p1;
+        ps4[e & 3] += p0 + p1;
         r[e] = pack_bf16x2(p0, p1);
       }
+      const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
       if (__any_sync(0xffffffffu, resc)) {
         // O must hold P(j-1) V(j-1) before it is rescaled
         if (j >= 1) {
