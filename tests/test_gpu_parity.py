@@ -629,6 +629,9 @@ PREFILL_CASES = {
     # up to 17 key tiles per query tile: the K/V ring wraps many times, and
     # the last CTA of each sequence has only its first query tile
     "h2_long": mi.scaled(mi.workload(3), B=2, h=2, L=None, lens=(1500, 2100)),
+    # mixed lengths with a one-token sequence between two long ones (most query
+    # tiles of the grid are empty for it)
+    "h32_mixed": mi.scaled(mi.workload(4), B=3, h=32, L=None, lens=(700, 1, 1300)),
 }
 
 
