@@ -8,6 +8,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace mla {
 namespace {
@@ -25,6 +26,9 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
                int d_c, int num_parts, void* __restrict__ o_lat, int o_dtype,
                float* __restrict__ lse_out) {
   __shared__ int s_first, s_count;
+  // scheduled while the decode finishes; its partials are read after it completes
+  tc::grid_dep_launch();
+  tc::grid_dep_wait();
   const int b = blockIdx.y;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (warp == 0) {
@@ -125,9 +129,8 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, const int
                            void* o_lat, int o_dtype, float* lse, cudaStream_t s) {
   if (num_parts > kMaxSplits) return cudaErrorInvalidValue;
   dim3 grid(ceil_div(h, kHeadsPerCta), B);
-  combine_kernel<<<grid, kThreads, 0, s>>>(o_part, lse_part, seq_lens, block_size, max_blocks, B,
-                                           h, d_c, num_parts, o_lat, o_dtype, lse);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(kThreads), 0, s, o_part, lse_part, seq_lens,
+                    block_size, max_blocks, B, h, d_c, num_parts, o_lat, o_dtype, lse);
 }
 
 }  // namespace mla

@@ -230,4 +230,26 @@ cudaError_t launch_paged_gather(const mla_kv_cache& kv, const int32_t* block_tab
                                 void* latent_out, void* rope_out, int32_t* status,
                                 cudaStream_t s);
 
+// ---------------------------------------------------------------------------
+// launches of the decode step's kernels: programmatic stream serialization, so
+// that a kernel's CTAs are scheduled while the previous kernel of the stream
+// finishes (each of these kernels calls grid_dep_wait before it reads memory
+// an earlier kernel may write, and grid_dep_launch at its start)
+// ---------------------------------------------------------------------------
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 }  // namespace mla

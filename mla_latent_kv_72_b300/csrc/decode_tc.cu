@@ -337,6 +337,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat,
   const uint32_t peer = rank ^ 1u;
   const int part = (blockIdx.x / 2) % p.num_parts;  // part of the block stream
   const int row0 = (blockIdx.x / 2) / p.num_parts * 128;  // first query row of this pair
+  // scheduled while the previous grid of the stream finishes; nothing is read
+  // from memory before that grid has completed
+  grid_dep_launch();
+  grid_dep_wait();
 
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8 * i; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -1373,9 +1377,8 @@ cudaError_t launch_variant(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope
   });
   if (r != 0) return r < 0 ? cudaErrorInvalidDevice : (cudaError_t)r;
   dim3 grid(2 * num_pairs);
-  decode_tc_kernel<kFp8><<<grid, Cfg<kFp8>::kThreads, Cfg<kFp8>::kSmemAlloc, s>>>(tm_lat, tm_rope,
-                                                                                 tm_q, prm);
-  return cudaGetLastError();
+  return launch_pdl(decode_tc_kernel<kFp8>, grid, dim3(Cfg<kFp8>::kThreads), Cfg<kFp8>::kSmemAlloc,
+                    s, tm_lat, tm_rope, tm_q, prm);
 }
 
 }  // namespace

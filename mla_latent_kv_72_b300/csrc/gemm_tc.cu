@@ -78,6 +78,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
   const int nk = p.K / kKChunk;
   const int nstage = p.nstage;
   const int kGStageBytes = p.stage_bytes;
+  grid_dep_launch();
 
   const uint32_t bars = sbase + nstage * kGStageBytes;   // full[4], empty[4], done
   auto full = [&](int i) { return bars + 8 * i; };
@@ -103,6 +104,20 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
   const uint32_t tmem = *tmem_holder;
   const long long lim = p.wait_limit;
   bool ok = true;
+  // this CTA's weight tiles into L2 while the previous grid of the stream
+  // finishes (a prefetch brings nothing into the CTA, and L2 stays coherent
+  // with that grid's writes); every read of memory comes after the wait
+  if (warp == 0 && lane == 0) {
+    for (int kc = 0; kc < nk; ++kc) {
+      if (kAMajorMN) {
+        tma_prefetch_2d(&tm_a, mt * 128, s * p.K + kc * kKChunk);
+        tma_prefetch_2d(&tm_a, mt * 128 + 64, s * p.K + kc * kKChunk);
+      } else {
+        tma_prefetch_2d(&tm_a, s * p.a_col_s + kc * kKChunk, s * p.a_row_s + mt * 128);
+      }
+    }
+  }
+  grid_dep_wait();
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -360,8 +375,7 @@ cudaError_t launch_absorb_q_tc(const void* q_nope, const void* q_rope, const int
   p.status = nullptr;
   p.wait_limit = 4000000000LL;
   dim3 grid(h, 512 / 128, ceil_div(B, nt));
-  head_gemm_kernel<true><<<grid, kGThreads, smem_bytes(p), s>>>(ta, tx, p);
-  return cudaGetLastError();
+  return launch_pdl(head_gemm_kernel<true>, grid, dim3(kGThreads), smem_bytes(p), s, ta, tx, p);
 }
 
 cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, int B, int h,
@@ -394,8 +408,7 @@ cudaError_t launch_out_proj_tc(const void* o_lat, const void* w_uv, void* out, i
   p.status = nullptr;
   p.wait_limit = 4000000000LL;
   dim3 grid(h, 1, ceil_div(B, nt));
-  head_gemm_kernel<false><<<grid, kGThreads, smem_bytes(p), s>>>(ta, tx, p);
-  return cudaGetLastError();
+  return launch_pdl(head_gemm_kernel<false>, grid, dim3(kGThreads), smem_bytes(p), s, ta, tx, p);
 }
 
 // ---------------------------------------------------------------------------

@@ -28,6 +28,21 @@ __device__ __forceinline__ uint32_t elect_one() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch (sm_90 and later)
+// ---------------------------------------------------------------------------
+
+// Wait until the grid that precedes this one in the stream has completed and
+// its memory operations are visible; a no-op when this grid was launched
+// without programmatic stream serialization.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid in the stream to be scheduled now (it still waits in
+// its own grid_dep_wait for this grid to complete).
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 
