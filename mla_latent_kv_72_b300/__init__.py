@@ -10,6 +10,8 @@ from .binding import (  # noqa: F401
     MLA_BF16,
     MLA_F32,
     MLA_FP8E4M3,
+    MLA_MAX_PARTS,
+    MLA_MAX_Q_LEN,
     MLAError,
     KVCache,
     dtype_code,

@@ -24,6 +24,9 @@ MLA_DEV_BAD_BLOCK = 1
 MLA_DEV_BAD_LENGTH = 2
 MLA_DEV_WAIT_TIMEOUT = 3
 
+MLA_MAX_PARTS = 1024
+MLA_MAX_Q_LEN = 8
+
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
 

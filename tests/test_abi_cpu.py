@@ -35,6 +35,14 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_binding_constants_match_the_header():
+    from mla_latent_kv_72_b300 import binding
+    defines = dict(re.findall(r"#define (MLA_[A-Z0-9_]+) (\d+)u?", open(HEADER).read()))
+    assert defines
+    for name, value in defines.items():
+        assert getattr(binding, name) == int(value), name
+
+
 def test_library_is_built_for_sm103a(lib):
     assert "arch=compute_103a,code=sm_103a" in " ".join(B.ARCH)
     assert os.path.getsize(M.library_path()) > 0
@@ -165,3 +173,83 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         binding.lib()
+
+
+def test_decode_multi_token_host_checks(lib):
+    f = lib.mla_decode_fwd_multi
+
+    def call(q_len=2, h=128, kv=None):
+        kv = _kv() if kv is None else kv
+        return f(A, M.MLA_BF16, ctypes.byref(kv), A, 4, A, 2, q_len, h, 2, 0.0, A, A, None, 0,
+                 None)
+
+    assert call(q_len=0) == -1
+    assert call(q_len=M.MLA_MAX_Q_LEN + 1) == -4
+    assert call(q_len=8, h=1024) == -4                 # q_len * h > 4096 query rows
+    assert call(kv=_kv(nblk=0)) == -1
+
+
+def test_cache_append_host_checks(lib):
+    f = lib.mla_cache_append
+    kv = _kv()
+
+    def call(c=A, kr=A, sdt=M.MLA_BF16, pos=A, B=2, table=A, maxb=4, kv=kv, theta=10000.0):
+        return f(c, kr, sdt, pos, B, table, maxb, ctypes.byref(kv), theta, None, None)
+
+    assert call(c=None) == -1
+    assert call(pos=None) == -1
+    assert call(B=0) == -1
+    assert call(maxb=0) == -1
+    assert call(theta=0.0) == -1
+    assert call(kv=_kv(nblk=0)) == -1
+    assert call(sdt=M.MLA_FP8E4M3) == -3
+    assert call(sdt=M.MLA_F32) == -3                   # f32 rows into a bf16 cache
+    kv8 = _kv(ldt=M.MLA_FP8E4M3, scale=A, lstride=512, rstride=64)
+    assert call(sdt=M.MLA_F32, kv=kv8) == -3           # FP8 latent takes bf16 rows
+    assert call(c=MIS) == -2
+
+
+def test_linear_and_fold_host_checks(lib):
+    ws = lib.mla_linear_workspace_bytes
+    # 7168-long contraction at 64 rows: eight 896-long splits of float32 partials
+    assert ws(64, 7168, 1536) == 8 * 64 * 1536 * 4
+    assert ws(64, 128, 128) == 0                       # one split: no workspace
+    assert ws(64, 100, 128) == 0 and ws(0, 128, 128) == 0
+    f = lib.mla_linear
+    assert f(None, A, A, 64, 128, 128, M.MLA_BF16, None, 0, None) == -1
+    assert f(A, A, A, 0, 128, 128, M.MLA_BF16, None, 0, None) == -1
+    assert f(A, A, A, 64, 128, 128, M.MLA_FP8E4M3, None, 0, None) == -3
+    assert f(A, A, A, 64, 100, 128, M.MLA_BF16, None, 0, None) == -4
+    assert f(A, A, A, 64, 128, 100, M.MLA_BF16, None, 0, None) == -4
+    assert f(A, MIS, A, 64, 128, 128, M.MLA_BF16, None, 0, None) == -2
+    need = 8 * 64 * 1536 * 4
+    assert f(A, A, A, 64, 7168, 1536, M.MLA_BF16, None, 0, None) == -1
+    assert f(A, A, A, 64, 7168, 1536, M.MLA_BF16, A, need - 1, None) == -1
+    assert f(A, A, A, 64, 7168, 1536, M.MLA_BF16, MIS, need, None) == -2
+    g = lib.mla_fold_uv_into_o
+    assert g(None, A, A, 4, 512, 128, 1024, None) == -1
+    assert g(A, A, A, 0, 512, 128, 1024, None) == -1
+    assert g(A, A, A, 4, 256, 128, 1024, None) == -4
+    assert g(A, A, MIS, 4, 512, 128, 1024, None) == -2
+
+
+def test_prefill_host_checks(lib):
+    q = lib.mla_prefill_query
+    assert q(None, A, A, 2, 100, 4, 10000.0, A, None) == -1
+    assert q(A, A, A, 0, 100, 4, 10000.0, A, None) == -1
+    assert q(A, A, A, 2, 100, 4, 0.0, A, None) == -1
+    assert q(A, MIS, A, 2, 100, 4, 10000.0, A, None) == -2
+    assert q(A, A, A, 2, 0, 4, 10000.0, A, None) == 0  # no rows: nothing to launch
+    f = lib.mla_prefill_fwd
+
+    def call(qp=A, kn=A, kr=A, v=A, cu=A, B=2, max_len=100, T=150, h=4, out=A,
+             odt=M.MLA_BF16):
+        return f(qp, kn, kr, v, cu, B, max_len, T, h, 0.0, out, odt, None, None, None)
+
+    assert call(qp=None) == -1
+    assert call(cu=None) == -1
+    assert call(B=0) == -1
+    assert call(T=0) == -1
+    assert call(odt=M.MLA_FP8E4M3) == -3
+    assert call(h=70000) == -4
+    assert call(kr=MIS) == -2
