@@ -417,8 +417,7 @@ def run_ours(args) -> None:
             ev[i][1].record(stream)
             dw.attend()
             ev[i][2].record(stream)
-            dw.combine()
-            dw.project()
+            dw.tail()
             if flush:
                 ev[i][3].record(stream)
         end.record(stream)
@@ -553,7 +552,7 @@ def run_ours(args) -> None:
         "kernels": breakdown,
         "append": append,
         "hidden": hidden,
-        "gpu_launches": 4 * n_st,
+        "gpu_launches": dw.launches_per_step() * n_st,
         "clocks": clocks,
         "settle_s": args.settle_s,
         "cpu_baseline": cpu,
@@ -648,27 +647,27 @@ def graph_time_us(fn, replays: int = 10, per_graph: int = 10) -> dict:
 
 def kernel_breakdown(dw, stream, flush: bool, scrub, steps: int = 50) -> dict:
     """Per-kernel device time of the step (after the timed region): events
-    between the four launches of each of `steps` further steps, so that every
+    between the launches of each of `steps` further steps, so that every
     kernel sees the cache state it has inside a step (the weights of absorb
-    and out_proj come from HBM after the decode's stream has passed)."""
+    and the projection come from HBM after the decode's stream has passed)."""
     import torch
-    names = ("mla_absorb_q", "mla_decode_fwd", "mla_combine", "mla_out_proj")
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    calls = [("mla_absorb_q", dw.absorb), ("mla_decode_fwd", dw.attend)]
+    if dw.fused_tail:
+        calls.append(("mla_combine_out_proj", dw.combine_project))
+    else:
+        calls += [("mla_combine", dw.combine), ("mla_out_proj", dw.project)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+          for _ in range(steps)]
     for i in range(steps):
         if flush:
             scrub.fill_(float(i))
         ev[i][0].record(stream)
-        dw.absorb()
-        ev[i][1].record(stream)
-        dw.attend()
-        ev[i][2].record(stream)
-        dw.combine()
-        ev[i][3].record(stream)
-        dw.project()
-        ev[i][4].record(stream)
+        for k, (_, fn) in enumerate(calls):
+            fn()
+            ev[i][k + 1].record(stream)
     torch.cuda.synchronize()
     out = {}
-    for k, n in enumerate(names):
+    for k, (n, _) in enumerate(calls):
         us = [e[k].elapsed_time(e[k + 1]) * 1e3 for e in ev]
         out[n] = {"median_us": statistics.median(us), "min_us": min(us)}
     out["steps"] = steps

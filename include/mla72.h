@@ -301,6 +301,28 @@ int mla_out_proj(const void* o_lat, const void* w_uv, void* out, int B, int h, i
                  int d_v, int in_dtype, int out_dtype, void* stream);
 
 /*
+ * mla_combine_out_proj: mla_combine followed by mla_out_proj in one call,
+ * without the merged rows passing through memory (iotdigitaltwinplm.com, the
+ * absorbed decode listing; kexue.fm "From MHA, MQA, GQA to MLA", eq. mla-mqa,
+ * first line: the latent output of head s goes through W_v^(s)):
+ *   o_lat[b, s, :] = the merge of mla_combine (same arithmetic and slot
+ *                    order: equal to mla_combine's output bit for bit)
+ *   out[b, s, v]   = sum_c bf16(o_lat[b, s, c]) w_uv[s, v, c]   (float32 accumulation)
+ *   o_part, lse_part, seq_lens, block_size, max_blocks_per_seq, num_parts: as
+ *                    for mla_combine (those of the decode call)
+ *   w_uv [h, d_v, d_c] bf16; out [B, h, d_v] in out_dtype (MLA_F32 or MLA_BF16)
+ *   o_lat [B, h, d_c] in o_dtype, or NULL (not written); lse [B, h] or NULL
+ *   dev_status: MLA_DEV_WAIT_TIMEOUT is or-ed in if a bounded wait gave up
+ *                    (may be NULL)
+ * Supported: d_c = 512, d_v = 128, h <= 65535.
+ */
+int mla_combine_out_proj(const float* o_part, const float* lse_part, const int32_t* seq_lens,
+                         int block_size, int max_blocks_per_seq, int B, int h, int d_c,
+                         int num_parts, const void* w_uv, int d_v, void* out, int out_dtype,
+                         void* o_lat, int o_dtype, float* lse, int32_t* dev_status,
+                         void* stream);
+
+/*
  * The hidden-state boundary of the step: the query side starts from the
  * hidden state x_t through the compressed query (kexue.fm "Part 3": the
  * query is also low-rank, c'_t = x_t W_c', and each head's query is read off

@@ -22,6 +22,7 @@ from .binding import (  # noqa: F401
     mla_cache_append,
     mla_cache_fill,
     mla_combine,
+    mla_combine_out_proj,
     mla_decode_fwd,
     mla_decode_fwd_multi,
     mla_decode_num_partials,

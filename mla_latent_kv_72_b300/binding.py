@@ -32,7 +32,7 @@ _LIB = None
 
 EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_version", "mla_cache_bytes_per_token", "mla_absorb_q",
-    "mla_decode_num_partials", "mla_decode_fwd", "mla_decode_fwd_multi", "mla_combine", "mla_decode_attend_noalloc",
+    "mla_decode_num_partials", "mla_decode_fwd", "mla_decode_fwd_multi", "mla_combine", "mla_combine_out_proj", "mla_decode_attend_noalloc",
     "mla_out_proj", "mla_cache_fill", "mla_cache_append", "mla_paged_gather",
     "mla_linear_workspace_bytes", "mla_linear", "mla_fold_uv_into_o", "mla_prefill_query",
     "mla_prefill_fwd",
@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
         "mla_decode_fwd_multi": (i32, [vp, i32, kvp, vp, i32, vp, i32, i32, i32, i32, f32, vp, vp,
                                        vp, u32, vp]),
         "mla_combine": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp]),
+        "mla_combine_out_proj": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, vp, i32,
+                                       vp, i32, vp, vp, vp]),
         "mla_decode_attend_noalloc": (i32, [vp, i32, kvp, vp, i32, vp, i32, i32, i32, f32, vp, i32,
                                             vp, vp, vp]),
         "mla_out_proj": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
@@ -227,6 +229,20 @@ def mla_combine(o_part, lse_part, seq_lens, block_size, max_blocks_per_seq, num_
         B, h, d_c, int(num_parts), _ptr(o_lat), dtype_code(o_lat.dtype), _ptr(lse),
         _stream(stream)))
     return o_lat
+
+
+def mla_combine_out_proj(o_part, lse_part, seq_lens, block_size, max_blocks_per_seq, num_parts,
+                         w_uv, out, o_lat=None, lse=None, dev_status=None, stream=None):
+    """out [B, h, d_v] = the merged partials through W_UV (see mla72.h); o_lat
+    [B, h, d_c] and lse [B, h] are written when given."""
+    B, h, d_v = out.shape
+    d_c = w_uv.shape[2]
+    _check("mla_combine_out_proj", lib().mla_combine_out_proj(
+        _ptr(o_part), _ptr(lse_part), _ptr(seq_lens), int(block_size), int(max_blocks_per_seq),
+        B, h, d_c, int(num_parts), _ptr(w_uv), d_v, _ptr(out), dtype_code(out.dtype),
+        _ptr(o_lat), dtype_code(o_lat.dtype) if o_lat is not None else 0, _ptr(lse),
+        _ptr(dev_status), _stream(stream)))
+    return out
 
 
 def mla_decode_attend_noalloc(q_cat, kv: KVCache, block_table, seq_lens, num_parts, o_lat,

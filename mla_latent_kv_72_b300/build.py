@@ -16,7 +16,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libmla72.so")
 
 SOURCES = ["api.cu", "absorb_q.cu", "decode_simt.cu", "decode_tc.cu", "gemm_tc.cu",
-           "combine.cu", "out_proj.cu", "cache.cu", "noalloc.cu", "prefill_tc.cu"]
+           "combine.cu", "out_proj.cu", "cache.cu", "noalloc.cu", "prefill_tc.cu",
+           "combine_proj.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

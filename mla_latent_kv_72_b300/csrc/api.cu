@@ -39,6 +39,15 @@ int check_cache(const mla_kv_cache* kv) {
 
 }  // namespace
 
+namespace mla {
+// defined in combine_proj.cu
+cudaError_t launch_combine_out_proj(const float* o_part, const float* lse_part,
+                                    const int32_t* seq_lens, int block_size, int max_blocks,
+                                    int B, int h, int num_parts, const void* w_uv, void* out,
+                                    int out_dtype, void* o_lat, int o_dtype, float* lse,
+                                    int32_t* status, cudaStream_t s);
+}  // namespace mla
+
 extern "C" {
 
 const char* mla_status_string(int status) {
@@ -163,6 +172,24 @@ int mla_combine(const float* o_part, const float* lse_part, const int32_t* seq_l
   return from_cuda(mla::launch_combine(o_part, lse_part, seq_lens, block_size,
                                        max_blocks_per_seq, B, h, d_c, num_parts, o_lat, o_dtype,
                                        lse, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_combine_out_proj(const float* o_part, const float* lse_part, const int32_t* seq_lens,
+                         int block_size, int max_blocks_per_seq, int B, int h, int d_c,
+                         int num_parts, const void* w_uv, int d_v, void* out, int out_dtype,
+                         void* o_lat, int o_dtype, float* lse, int32_t* dev_status,
+                         void* stream) {
+  if (!o_part || !lse_part || !seq_lens || !w_uv || !out) return MLA_ERR_ARG;
+  if (B <= 0 || h <= 0 || num_parts <= 0 || block_size <= 0 || max_blocks_per_seq <= 0)
+    return MLA_ERR_ARG;
+  if (!is_float_dtype(out_dtype) || (o_lat && !is_float_dtype(o_dtype))) return MLA_ERR_DTYPE;
+  if (d_c != 512 || d_v != 128 || h > 65535 || num_parts > MLA_MAX_PARTS) return MLA_ERR_SHAPE;
+  if (!aligned16(o_part) || !aligned16(w_uv) || (o_lat && !aligned16(o_lat)))
+    return MLA_ERR_ALIGN;
+  if (!mla::tc_device()) return MLA_ERR_DEVICE;
+  return from_cuda(mla::launch_combine_out_proj(
+      o_part, lse_part, seq_lens, block_size, max_blocks_per_seq, B, h, num_parts, w_uv, out,
+      out_dtype, o_lat, o_dtype, lse, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 int mla_out_proj(const void* o_lat, const void* w_uv, void* out, int B, int h, int d_c, int d_v,

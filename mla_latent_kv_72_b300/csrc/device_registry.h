@@ -65,6 +65,7 @@ enum SetupKey : int {
   kSetupGemmK = 3,        // ... of the per-head GEMM, K-major A (out_proj)
   kSetupAppend = 4,       // ... of the cache-append kernel
   kSetupPrefill = 5,      // ... of the prefill attention kernel
+  kSetupCombineProj = 6,  // ... of the merged combine + output projection kernel
   kSetupKeyCount
 };
 

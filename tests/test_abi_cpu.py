@@ -253,3 +253,24 @@ def test_prefill_host_checks(lib):
     assert call(odt=M.MLA_FP8E4M3) == -3
     assert call(h=70000) == -4
     assert call(kr=MIS) == -2
+
+
+def test_combine_out_proj_host_checks(lib):
+    f = lib.mla_combine_out_proj
+
+    def call(op=A, seq=A, B=2, h=4, d_c=512, parts=2, w=A, d_v=128, out=A, odt=M.MLA_BF16,
+             olat=None, oldt=M.MLA_BF16):
+        return f(op, A, seq, 64, 4, B, h, d_c, parts, w, d_v, out, odt, olat, oldt, None, None,
+                 None)
+
+    assert call(op=None) == -1
+    assert call(w=None) == -1
+    assert call(B=0) == -1
+    assert call(parts=0) == -1
+    assert call(odt=M.MLA_FP8E4M3) == -3
+    assert call(olat=A, oldt=M.MLA_FP8E4M3) == -3
+    assert call(d_c=256) == -4
+    assert call(d_v=64) == -4
+    assert call(parts=2000) == -4
+    assert call(w=MIS) == -2
+    assert call(olat=MIS) == -2

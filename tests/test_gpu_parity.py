@@ -658,3 +658,42 @@ def test_prefill_matches_oracle(name):
                                 inp["w_uv"], c, kr)
         assert rel_err(out[cu[b]:cu[b + 1]], r["out"]) <= TOL["bf16"], b
         assert abs_err(lse[cu[b]:cu[b + 1]], r["lse"]) <= TOL["bf16"], b
+
+
+COMBINE_PROJ_CASES = {
+    "v3_b3": (3, dict(B=3, L=900), None),
+    # two batch tiles of 64 rows, the second ragged; few parts per sequence
+    "v3_b70": (3, dict(B=70, h=16, L=700), 40),
+    "paged_b5": (4, dict(B=5, h=16, L_range=(1, 2000)), 37),
+    "fp8_b2_256parts": (5, dict(B=2, L=20000), 256),
+}
+
+
+def _same_bits(a, b):
+    bits = torch.int16 if a.element_size() == 2 else torch.int32
+    return a.shape == b.shape and torch.equal(a.view(bits), b.view(bits))
+
+
+@pytest.mark.parametrize("case", list(COMBINE_PROJ_CASES))
+def test_combine_out_proj_equals_the_pair(case):
+    """mla_combine_out_proj: o_lat and lse bit for bit equal to mla_combine's,
+    out equal to mla_out_proj's to float32 rounding, and to the oracle."""
+    idx, kw, parts = COMBINE_PROJ_CASES[case]
+    w = mi.scaled(mi.workload(idx), **kw)
+    dw = make(w, num_parts=parts)
+    dw.absorb()
+    dw.attend()
+    dw.combine()
+    dw.project()
+    torch.cuda.synchronize()
+    ref = (dw.o_lat.clone(), dw.lse.clone(), dw.out.clone())
+    for t in (dw.o_lat, dw.lse, dw.out):
+        t.fill_(float("nan"))
+    dw.combine_project()
+    torch.cuda.synchronize()
+    assert dw.check_status() == 0
+    assert _same_bits(dw.o_lat, ref[0]) and _same_bits(dw.lse, ref[1])
+    o, r = dw.out.float().cpu().numpy(), ref[2].float().cpu().numpy()
+    assert np.all(np.isfinite(o))
+    assert np.abs(o - r).max() <= 1e-5 * np.abs(r).max()
+    compare(w, dw, range(min(w.B, 2)), [0, 7], TOL["bf16"])
