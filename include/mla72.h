@@ -30,6 +30,11 @@
  *     cudaMalloc or PyTorch allocation is), the tensor-core decode moves them
  *     with 32-byte accesses; otherwise with 16-byte ones, same results.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - mla_absorb_q, mla_decode_fwd(_multi), mla_combine, mla_combine_out_proj
+ *     and mla_out_proj launch with programmatic stream serialization: their
+ *     CTAs may be scheduled while the previous kernel of the stream finishes,
+ *     and they read no memory before that kernel has completed, so stream
+ *     order holds as for any launch.
  *   - Host-side argument checks run before anything is launched; on failure
  *     the call returns a negative mla_status and launches nothing.
  *   - A CUDA launch error is returned as MLA_ERR_LAUNCH.
